@@ -1,0 +1,353 @@
+"""Benchmark of one MoE layer pass (forward + backward) on GB300, printing one JSON line.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+A step is one pass of the whole hot path over one batch: routing, counting/index generation,
+permutation, grouped SwiGLU GEMM, combine, and the full backward (combine/routing backward,
+grouped GEMM backward incl. weight gradients, un-permute). Inputs are seeded synthetic tensors
+resident in HBM before timing starts; the expert weights (768 MiB at the default workload) and the
+grouped activations exceed the 129 MB L2, so no flush is needed between steps.
+
+Under torchrun (N > 1) every rank runs an independent replica on its own GPU (the layer has no
+exchange step on one node here): weak scaling, max-over-ranks time, value = all ranks' tokens / time.
+
+--impl reference times the fp64 CPU oracle (as it stands) on a bounded token sample of the same
+workload on the host cores; on N > 1 only rank 0 runs it.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "MoE layer fwd+bwd tokens/s (E=64,k=8,d=2048); grouped-GEMM % BF16 peak"
+DEFAULT_WORKLOAD = "fwdbwd_t8192"
+
+
+def _peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as fh:
+            p = json.load(fh)
+        return dict(hbm=p["hbm_gbs"], bf16=p["bf16_tflops"], bf16_sustained=p.get("bf16_tflops_sustained"),
+                    src="measured")
+    except Exception:
+        return dict(hbm=6800.0, bf16=1900.0, bf16_sustained=1700.0, src="fallback")
+
+
+def _dist():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples during the timed region."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        self.lines = []
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except Exception:
+                self.proc.kill()
+                out = ""
+            self.lines = [ln for ln in out.splitlines() if ln.strip()]
+
+    def summary(self):
+        if not getattr(self, "lines", None):
+            return None
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+            except (ValueError, IndexError):
+                continue
+            for nm, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    import moe_inputs
+    from mixture_experts_layer_histogram_gb300 import MoELayer
+    from mixture_experts_layer_histogram_gb300 import _lib as L
+
+    world, rank, local = _dist()
+    if world > 1:
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", local if world > 1 else 0)
+    torch.cuda.set_device(dev)
+    w = moe_inputs.WORKLOADS[args.workload]
+    assert w.backward, "the bench times forward + backward"
+    inp = moe_inputs.make_all(w, dev)
+    x, logits, wgu, wd, g = inp["x"], inp["logits"], inp["w_gate_up"], inp["w_down"], inp["g"]
+    layer = MoELayer(w.T, w.d, w.E, w.k, w.f, w.torch_dtype, dev)
+    stream = torch.cuda.current_stream(dev)
+    M = w.T * w.k
+    gemm_flop = 18.0 * M * w.d * w.f
+
+    def step(ev=None):
+        if ev is None:
+            layer.forward(x, logits, wgu, wd)
+            layer.backward(g, wgu, wd)
+            return
+        # events around each C-ABI call, on the stream the kernels are launched on
+        ev[0].record(stream)
+        L.moe_route_topk(logits, w.k, layer.topk_idx, layer.topk_w)
+        ev[1].record(stream)
+        L.moe_count_index(layer.topk_idx, w.E, layer.counts, layer.offsets, layer.tile_offsets, layer.row_of_slot,
+                          layer.token_of_row, layer.ws_index)
+        ev[2].record(stream)
+        L.moe_permute(x, w.k, w.E, layer.row_of_slot, layer.counts, layer.tile_offsets, layer.x_perm)
+        ev[3].record(stream)
+        L.moe_grouped_ffn_fwd(layer.x_perm, wgu, wd, layer.tile_offsets, layer.ab, layer.h, layer.y_perm,
+                              layer.ws_ffn)
+        ev[4].record(stream)
+        L.moe_combine_fwd(layer.y_perm, layer.topk_w, layer.row_of_slot, w.T, w.k, layer.out)
+        ev[5].record(stream)
+        L.moe_combine_bwd(g, layer.y_perm, layer.topk_w, layer.topk_idx, layer.row_of_slot, layer.counts,
+                          layer.tile_offsets, w.E, layer.dy_perm, layer.d_topk_w, layer.d_logits)
+        ev[6].record(stream)
+        L.moe_grouped_ffn_bwd(layer.dy_perm, layer.x_perm, layer.ab, layer.h, wgu, wd, layer.tile_offsets, layer.dab,
+                              layer.dx_perm, layer.dw_gate_up, layer.dw_down, layer.ws_ffn)
+        ev[7].record(stream)
+        L.moe_combine_fwd(layer.dx_perm, None, layer.row_of_slot, w.T, w.k, layer.dx)
+        ev[8].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    st = layer.status()
+    if st != (0, 0):
+        raise RuntimeError(f"device status after warm-up: {st}")
+
+    names = ["route_topk", "count_index", "permute", "grouped_ffn_fwd", "combine_fwd", "combine_bwd",
+             "grouped_ffn_bwd", "unpermute"]
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(9)] for _ in range(args.steps)]
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    with ClockSampler(dev.index) as clk:
+        t_start.record(stream)
+        for i in range(args.steps):
+            step(evs[i])
+        t_end.record(stream)
+        torch.cuda.synchronize(dev)
+    if world > 1:
+        dist.barrier()
+    elapsed_ms = t_start.elapsed_time(t_end)
+    if world > 1:
+        tt = torch.tensor([elapsed_ms], device=dev, dtype=torch.float64)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        elapsed_ms = float(tt.item())
+    per = {n: statistics.mean(evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(args.steps))
+           for j, n in enumerate(names)}
+    st = layer.status()
+    if st != (0, 0):
+        raise RuntimeError(f"device status after timing: {st}")
+
+    # ---------------------------------------------------------------- end to end: host buffers
+    pin = dict(x=x.cpu().pin_memory(), logits=logits.cpu().pin_memory(), g=g.cpu().pin_memory())
+    host_out = {k: torch.empty(v.shape, dtype=v.dtype).pin_memory()
+                for k, v in (("out", layer.out), ("dx", layer.dx), ("d_logits", layer.d_logits))}
+    dx_, dl_, dg_ = torch.empty_like(x), torch.empty_like(logits), torch.empty_like(g)
+    h2d = sum(v.numel() * v.element_size() for v in pin.values())
+    d2h = sum(v.numel() * v.element_size() for v in host_out.values())
+
+    def e2e_step():
+        dx_.copy_(pin["x"], non_blocking=True)
+        dl_.copy_(pin["logits"], non_blocking=True)
+        dg_.copy_(pin["g"], non_blocking=True)
+        layer.forward(dx_, dl_, wgu, wd)
+        layer.backward(dg_, wgu, wd)
+        host_out["out"].copy_(layer.out, non_blocking=True)
+        host_out["dx"].copy_(layer.dx, non_blocking=True)
+        host_out["d_logits"].copy_(layer.d_logits, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize(dev)
+    if world > 1:
+        dist.barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = e0.elapsed_time(e1)
+    if world > 1:
+        tt = torch.tensor([e2e_ms], device=dev, dtype=torch.float64)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        e2e_ms = float(tt.item())
+
+    cpu_base = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu_base = oracle_baseline(w, inp, budget_s=args.cpu_seconds)
+    if world > 1:
+        dist.destroy_process_group()
+    if rank != 0:
+        return None
+
+    peaks = _peaks()
+    ms = elapsed_ms / args.steps
+    gemm_ms = per["grouped_ffn_fwd"] + per["grouped_ffn_bwd"]
+    achieved = gemm_flop / (gemm_ms * 1e-3) / 1e12
+    peak = peaks["bf16_sustained"] or peaks["bf16"]
+    mem_bytes = {   # algorithmic bytes per call (bf16 rows; indices 4 B)
+        "permute": (w.T * w.d + M * w.d) * 2 + M * 4,
+        "combine_fwd": (M * w.d + w.T * w.d) * 2 + M * 8,
+        "combine_bwd": (w.T * w.d + 2 * M * w.d) * 2 + M * 16 + w.T * w.E * 4,
+        "unpermute": (M * w.d + w.T * w.d) * 2 + M * 4,
+    }
+    kern = {n: {"ms": round(v, 4)} for n, v in per.items()}
+    for n, b in mem_bytes.items():
+        kern[n]["GBps"] = round(b / (per[n] * 1e-3) / 1e9, 1)
+        kern[n]["frac_hbm"] = round(b / (per[n] * 1e-3) / 1e9 / peaks["hbm"], 3)
+    kern["grouped_ffn_fwd"]["TFLOPs"] = round(6.0 * M * w.d * w.f / (per["grouped_ffn_fwd"] * 1e-3) / 1e12, 1)
+    kern["grouped_ffn_bwd"]["TFLOPs"] = round(12.0 * M * w.d * w.f / (per["grouped_ffn_bwd"] * 1e-3) / 1e12, 1)
+    value = world * w.T * args.steps / (elapsed_ms * 1e-3)
+    line = {
+        "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms, 4), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded; see moe_inputs.py)",
+        "config": {"workload": w.name, "T": w.T, "d": w.d, "E": w.E, "k": w.k, "f": w.f, "routing": w.routing,
+                   "pass": "fwd+bwd", "parallelism": f"replicas x{world}",
+                   "l2": "inputs larger than L2 (expert weights 768 MiB, grouped activations > 129 MB); no flush"},
+        "roofline": {"kernel": "grouped SwiGLU GEMM (6 tcgen05 launches per step: fwd GATEUP, DOWN; bwd DH, "
+                               "WGRAD down, DGRAD, WGRAD gate/up)",
+                     "bound": "tensor", "achieved": round(achieved, 1), "peak": peak, "unit": "TFLOP/s",
+                     "frac": round(achieved / peak, 3),
+                     "peak_kind": f"{peaks['src']} bf16 dense, sustained (kernel timed inside a long step)",
+                     "algorithmic_flop_per_step": gemm_flop, "traffic": None},
+        "kernels": kern,
+        "e2e": {"value": round(world * w.T * args.steps / (e2e_ms * 1e-3), 1), "unit": "tokens/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": layer.launches(True) * args.steps,
+        "clocks": clk.summary(),
+        "cpu_baseline": cpu_base,
+    }
+    return line
+
+
+def oracle_baseline(w, inp, budget_s=15.0, per_step_s=None):
+    """Time the fp64 oracle (forward + backward incl. weight gradients) on a bounded token sample."""
+    import torch
+
+    import oracle
+    cpu = {k: v.detach().cpu() for k, v in inp.items()}
+
+    def run(n):
+        sl = slice(0, n)
+        x, lg, g = cpu["x"][sl].contiguous(), cpu["logits"][sl].contiguous(), cpu["g"][sl].contiguous()
+        t0 = time.perf_counter()
+        idx, wt = oracle.route_topk(lg, w.k)
+        oracle.index(idx, w.E, 128)
+        oracle.moe_tokens(x, idx, wt, cpu["w_gate_up"], cpu["w_down"], g)
+        oracle.moe_dweights(x, idx, wt, cpu["w_gate_up"], cpu["w_down"], g)
+        return time.perf_counter() - t0
+
+    t_probe = run(4)
+    n = max(4, min(w.T, int(4 * budget_s / max(t_probe, 1e-3))))
+    dt = run(n)
+    return {"value": round(n / dt, 3), "unit": "tokens/s", "cores": oracle.num_threads(), "kind": "oracle",
+            "sample": f"first {n} tokens of {w.name}, fwd+bwd incl. dW, {dt:.1f} s wall"}
+
+
+def run_reference(args):
+    world, rank, local = _dist()
+    if rank != 0:
+        return None
+    import torch
+
+    import moe_inputs
+    import oracle
+    w = moe_inputs.WORKLOADS[args.workload]
+    inp = moe_inputs.make_all(w, "cpu")
+    cpu = inp
+    n = args.ref_tokens
+
+    def one():
+        sl = slice(0, n)
+        x, lg, g = cpu["x"][sl].contiguous(), cpu["logits"][sl].contiguous(), cpu["g"][sl].contiguous()
+        idx, wt = oracle.route_topk(lg, w.k)
+        oracle.index(idx, w.E, 128)
+        oracle.moe_tokens(x, idx, wt, cpu["w_gate_up"], cpu["w_down"], g)
+        oracle.moe_dweights(x, idx, wt, cpu["w_gate_up"], cpu["w_down"], g)
+
+    for _ in range(args.warmup):
+        one()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        one()
+    dt = time.perf_counter() - t0
+    value = n * args.steps / dt
+    cb = {"value": round(value, 3), "unit": "tokens/s", "cores": oracle.num_threads(), "kind": "oracle",
+          "sample": f"first {n} tokens of {w.name} per step, fwd+bwd incl. dW"}
+    return {"impl": "reference", "metric": METRIC, "value": round(value, 3), "unit": "tokens/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt / args.steps * 1e3, 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (seeded; see moe_inputs.py)",
+            "config": {"workload": w.name, "T": w.T, "d": w.d, "E": w.E, "k": w.k, "f": w.f, "routing": w.routing,
+                       "pass": "fwd+bwd", "parallelism": "host cores"},
+            "cpu_baseline": cb,
+            "e2e": {"value": round(value, 3), "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--ref-tokens", type=int, default=8)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("at least 3 warm-up steps")
+    line = run_reference(args) if args.impl == "reference" else run_ours(args)
+    if line is not None:
+        print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,180 @@
+/*
+ * moe.h - C ABI of libmoe: the single-GPU hot path of one Mixture-of-Experts layer's expert
+ * computation (GB300 / sm_103a), forward and backward.
+ *
+ * Source of the method: "Scalable Pretraining of Large MoE LMs on Aurora" (arXiv 2604.00785).
+ * Its FastSparseMoE module (brief, section 核心方法) counts tokens per expert and generates their
+ * indices with GPU kernels, then merges every expert's FFN into one grouped GEMM; the summary page
+ * (section 关键设计) adds optimised matmul and activation kernels, and both pages report the module
+ * on the forward and backward pass (brief, sections 为什么值得记录 / 关键结果). The pages fix
+ * neither the router nor the activation; this library implements softmax top-k routing with
+ * renormalised weights (ties to the lower expert id) and SwiGLU experts.
+ *
+ * Layer, per token t with input x_t [d], router logits L[t, :] [E], grad_out g_t [d]:
+ *   S_t      = the k experts with largest L[t,e], ordered by (L desc, e asc)
+ *   w_{t,e}  = softmax of L[t, S_t]                       (topk_idx / topk_w, slot j = t*k + j)
+ *   out_t    = sum_{e in S_t} w_{t,e} * Wd[e] (silu(Wg[e] x_t) * (Wu[e] x_t))
+ *
+ * Conventions for every call:
+ *   - Returns MOE_OK (0) or a negative moe_status. Argument errors are detected on the host before
+ *     anything is enqueued. Calls are asynchronous on `stream` (NULL = legacy default stream) and
+ *     never synchronise, except moe_read_status.
+ *   - Every pointer named like a tensor is DEVICE memory owned by the caller, contiguous, row-major,
+ *     16-byte aligned. The library allocates nothing and keeps no per-call state between calls.
+ *   - dtype: MOE_F32 or MOE_BF16 for x, weights, grad_out and every grouped activation buffer.
+ *     Logits, routing weights and their gradients are always fp32; indices are int32.
+ *   - Calls that can detect an error on the device (a bad expert id, a wait that ran out) write a
+ *     status word at the start of their workspace `ws`; read it with moe_read_status(ws, stream).
+ *
+ * Grouped layout. The permuted ("grouped") buffers hold the routed rows expert by expert. Expert
+ * e's rows start at row tile_offsets[e] * MOE_GROUP_ROWS and follow increasing slot index (so
+ * increasing token index); the rows after the last token of an expert up to the next multiple of
+ * MOE_GROUP_ROWS are padding and are kept at zero. Every grouped buffer has
+ * rows_max = moe_grouped_rows_max(T, k, E) rows; rows from tile_offsets[E] * MOE_GROUP_ROWS on are
+ * never touched. With this layout every grouped-GEMM tile belongs to one expert and is full.
+ */
+#ifndef MOE_LAYER_H_
+#define MOE_LAYER_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t. */
+typedef struct CUstream_st *moe_stream_t;
+
+#define MOE_VERSION 100         /* 1.0.0 */
+#define MOE_GROUP_ROWS 128      /* rows per grouped-GEMM tile; each expert's row group is aligned to it */
+#define MOE_MAX_EXPERTS 256
+#define MOE_MAX_TOPK 16
+
+enum moe_dtype { MOE_F32 = 0, MOE_BF16 = 1 };
+
+enum moe_status {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = -1,     /* null pointer, bad size, misalignment, workspace too small */
+  MOE_ERR_UNSUPPORTED = -2,     /* shape or dtype outside what a kernel supports (see each call) */
+  MOE_ERR_CUDA = -3,            /* a CUDA runtime call or launch failed */
+  MOE_ERR_DEVICE_TIMEOUT = -4,  /* a bounded device-side wait ran out (device status word) */
+  MOE_ERR_BAD_INDEX = -5        /* an expert id outside [0, E) was seen (device status word) */
+};
+
+/* ---------------------------------------------------------------------------------------------
+ * Routing (brief, section 核心方法: expert selection feeding the token counting step).
+ * logits [T, E] fp32 -> topk_idx [T, k] int32 (ordered by logit desc, lower id on ties; -0 == +0),
+ *                       topk_w [T, k] fp32 = softmax over the k selected logits.
+ * Requires 1 <= E <= MOE_MAX_EXPERTS, 1 <= k <= min(E, MOE_MAX_TOPK), T >= 0. Logits must be
+ * finite (non-finite input gives unspecified selections). No workspace, no device status.
+ */
+int moe_route_topk(const float *logits, int T, int E, int k, int32_t *topk_idx, float *topk_w,
+                   moe_stream_t stream);
+
+/* Rows of every grouped buffer: round_up(T*k + E*(MOE_GROUP_ROWS-1), MOE_GROUP_ROWS). */
+int64_t moe_grouped_rows_max(int T, int k, int E);
+
+/* ---------------------------------------------------------------------------------------------
+ * Token counting and index generation (brief, section 核心方法: "GPU kernels for token counting and
+ * index generation"). A stable counting sort of the T*k slots by expert id, in two kernels:
+ * a warp-aggregated histogram, then a per-expert decoupled look-back scan over blocks and a
+ * stable scatter.
+ *   topk_idx     [T*k] int32 in [0, E)
+ *   counts       [E]   rows routed to each expert
+ *   offsets      [E+1] exclusive scan of counts (offsets[E] = T*k)
+ *   tile_offsets [E+1] exclusive scan of ceil(counts[e] / MOE_GROUP_ROWS)
+ *   row_of_slot  [T*k] grouped row of slot t*k+j: tile_offsets[e]*MOE_GROUP_ROWS + (number of
+ *                      earlier slots routed to the same expert)
+ *   token_of_row [rows_max] token of each grouped row, -1 on padding rows
+ * ws: moe_count_index_workspace_size(T, k, E) bytes of device memory, any content (the call
+ * resets what it needs). Device errors: MOE_ERR_BAD_INDEX (such slots get row_of_slot = -1 and
+ * are not counted), MOE_ERR_DEVICE_TIMEOUT (the look-back wait is bounded to about 0.2 s).
+ * Fault-injection hook (for tests of the bounded wait): the int32 at byte offset
+ * moe_count_index_hook_offset(E) of ws is read on the device by the call. If it holds b + 1
+ * (b >= 0), scan block b withholds its published prefix, so its successor's bounded wait runs out
+ * and the call reports MOE_ERR_DEVICE_TIMEOUT. The call clears the hook; leave it 0 otherwise.
+ */
+size_t moe_count_index_workspace_size(int T, int k, int E);
+size_t moe_count_index_hook_offset(int E);
+int moe_count_index(const int32_t *topk_idx, int T, int k, int E, int32_t *counts, int32_t *offsets,
+                    int32_t *tile_offsets, int32_t *row_of_slot, int32_t *token_of_row, void *ws,
+                    size_t ws_bytes, moe_stream_t stream);
+
+/* ---------------------------------------------------------------------------------------------
+ * Token permutation into the grouped layout (the consumer of the generated indices; brief,
+ * section 核心方法). x [T, d] -> x_perm [rows_max, d]: x_perm[row_of_slot[t*k+j]] = x[t]; padding
+ * rows of every expert are written with zeros. Each x row is read once and written k times.
+ * Requires d*sizeof(dtype) % 16 == 0. Slots whose row is outside [0, rows_max) are skipped.
+ */
+int moe_permute(const void *x, int dtype, int T, int d, int k, int E, const int32_t *row_of_slot,
+                const int32_t *counts, const int32_t *tile_offsets, int64_t rows_max, void *x_perm,
+                moe_stream_t stream);
+
+/* ---------------------------------------------------------------------------------------------
+ * Grouped expert FFN, forward (brief, section 核心方法: "Grouped GEMM merges the experts'
+ * computation"; summary page, section 关键设计: optimised matmul and activation).
+ *   x_perm    [rows_max, d]   grouped tokens
+ *   w_gate_up [E, 2f, d]      rows 0..f-1: gate projection Wg[e]; rows f..2f-1: up projection Wu[e]
+ *   w_down    [E, d, f]       Wd[e]
+ *   ab        [rows_max, 2f]  saved for backward: columns 0..f-1 a = x Wg^T, f..2f-1 b = x Wu^T
+ *   h         [rows_max, f]   saved: silu(a) * b
+ *   y_perm    [rows_max, d]   h Wd^T
+ * GEMM1 fuses the SwiGLU gate into its epilogue; GEMM2 is a plain grouped GEMM. bf16: tcgen05
+ * tensor cores, fp32 accumulation, outputs rounded to bf16; requires d % 256 == 0 and
+ * f % 256 == 0. fp32: SIMT fp32 FMA, any d, f >= 1. tile_offsets comes from moe_count_index.
+ * ws: moe_grouped_ffn_workspace_size(...) bytes (device status word). Padding rows produce zeros.
+ */
+size_t moe_grouped_ffn_workspace_size(int E, int d, int f, int64_t rows_max, int dtype, int backward);
+int moe_grouped_ffn_fwd(const void *x_perm, const void *w_gate_up, const void *w_down,
+                        const int32_t *tile_offsets, int E, int d, int f, int64_t rows_max, int dtype,
+                        void *ab, void *h, void *y_perm, void *ws, size_t ws_bytes, moe_stream_t stream);
+
+/* ---------------------------------------------------------------------------------------------
+ * Grouped expert FFN, backward (brief, sections 为什么值得记录 / 关键结果: the module is measured
+ * on the forward-backward pass). With dy = dy_perm (from moe_combine_bwd):
+ *   dab      [rows_max, 2f]  da = dh * b * s(a)(1 + a(1 - s(a))), db = dh * silu(a), dh = dy Wd[e]
+ *   dx_perm  [rows_max, d]   dab Wgu[e]
+ *   dw_down  [E, d, f]       sum over expert e's rows of dy^T h      (overwritten, not accumulated)
+ *   dw_gate_up [E, 2f, d]    sum over expert e's rows of dab^T x_perm (overwritten)
+ * Padding rows of dy_perm must be zero (moe_combine_bwd writes them so). Same dtype rules as the
+ * forward; gradients are written in the parameter dtype, accumulated in fp32.
+ */
+int moe_grouped_ffn_bwd(const void *dy_perm, const void *x_perm, const void *ab, const void *h,
+                        const void *w_gate_up, const void *w_down, const int32_t *tile_offsets, int E,
+                        int d, int f, int64_t rows_max, int dtype, void *dab, void *dx_perm,
+                        void *dw_gate_up, void *dw_down, void *ws, size_t ws_bytes, moe_stream_t stream);
+
+/* ---------------------------------------------------------------------------------------------
+ * Weighted un-permute (combine) back to token order:
+ *   out[t] = sum_j topk_w[t,j] * y_perm[row_of_slot[t*k+j]]   (fp32 accumulation in slot order)
+ * With topk_w == NULL the rows are summed unweighted: the backward of moe_permute
+ * (dx[t] = sum_j dx_perm[row_of_slot[t*k+j]]). out [T, d] in dtype. Same size rules as permute.
+ */
+int moe_combine_fwd(const void *y_perm, const float *topk_w, const int32_t *row_of_slot, int T, int d,
+                    int k, int64_t rows_max, int dtype, void *out, moe_stream_t stream);
+
+/* ---------------------------------------------------------------------------------------------
+ * Backward of the combine and of the routing weights, per token t with g = grad_out[t]:
+ *   dy_perm[row_of_slot[t*k+j]] = topk_w[t,j] * g                       (dtype; padding rows zeroed)
+ *   d_topk_w[t,j]  = <g, y_perm[row_of_slot[t*k+j]]>                     [T, k] fp32
+ *   d_logits[t,e]  = w_e (d_topk_w_e - sum_j w_j d_topk_w_j) for e in S_t, else 0    [T, E] fp32
+ * (the softmax-over-selected-logits backward; the selection itself is held fixed).
+ */
+int moe_combine_bwd(const void *grad_out, const void *y_perm, const float *topk_w, const int32_t *topk_idx,
+                    const int32_t *row_of_slot, const int32_t *counts, const int32_t *tile_offsets, int T,
+                    int d, int k, int E, int64_t rows_max, int dtype, void *dy_perm, float *d_topk_w,
+                    float *d_logits, moe_stream_t stream);
+
+/* ---------------------------------------------------------------------------------------------
+ * Synchronises `stream`, then returns the device status word at the start of a workspace used by
+ * moe_count_index or moe_grouped_ffn_*: MOE_OK or a negative moe_status. Not for the hot path.
+ */
+int moe_read_status(const void *ws, moe_stream_t stream);
+const char *moe_status_string(int status);
+int moe_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MOE_LAYER_H_ */

@@ -1,0 +1,8 @@
+"""Single-GPU MoE layer hot path for GB300 (sm_103a): softmax top-k routing, per-expert token
+counting and index generation, token permutation, grouped SwiGLU GEMM on tcgen05 tensor cores,
+and the weighted combine, forward and backward, behind the C ABI in include/moe.h."""
+from . import _lib
+from ._lib import MoeError
+from .layer import MoELayer
+
+__all__ = ["MoELayer", "MoeError", "_lib"]

@@ -1,0 +1,87 @@
+// Shared device/host helpers of libmoe (sm_103a). Nothing here is visible through the C ABI.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "moe.h"
+
+#define MOE_TRY_CUDA(expr)                 \
+  do {                                     \
+    cudaError_t err__ = (expr);            \
+    if (err__ != cudaSuccess) {            \
+      (void)cudaGetLastError();            \
+      return MOE_ERR_CUDA;                 \
+    }                                      \
+  } while (0)
+
+#define MOE_CHECK_LAUNCH() MOE_TRY_CUDA(cudaGetLastError())
+
+namespace moe {
+
+// Every workspace starts with this header (the device status word first).
+struct WsHeader {
+  int32_t status;        // first device-detected error (0 = none)
+  int32_t detail;        // extra information about it (e.g. the block that timed out)
+  int32_t armed;         // moe_count_index: look-back fault hook as consumed for this call (0 = off)
+  int32_t pad0;
+  uint32_t tickets[4];   // self-managed counters (reset by the call that uses them)
+  uint32_t pad1[8];
+};
+static_assert(sizeof(WsHeader) == 64, "workspace header is 64 bytes");
+
+constexpr uint64_t kWaitLimitNs = 200ull * 1000ull * 1000ull;   // bounded device waits: 0.2 s
+
+__device__ __forceinline__ uint64_t global_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// Record the first error only.
+__device__ __forceinline__ void report(WsHeader *ws, int code, int detail) {
+  if (ws == nullptr) return;
+  if (atomicCAS(&ws->status, 0, code) == 0) ws->detail = detail;
+}
+
+__device__ __forceinline__ float bf16_to_f(uint16_t u) { return __uint_as_float((uint32_t)u << 16); }
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);   // round to nearest even
+  return *reinterpret_cast<uint32_t *>(&v);
+}
+
+__device__ __forceinline__ void unpack_bf16x8(const uint4 &q, float *v) {
+  v[0] = __uint_as_float(q.x << 16); v[1] = __uint_as_float(q.x & 0xffff0000u);
+  v[2] = __uint_as_float(q.y << 16); v[3] = __uint_as_float(q.y & 0xffff0000u);
+  v[4] = __uint_as_float(q.z << 16); v[5] = __uint_as_float(q.z & 0xffff0000u);
+  v[6] = __uint_as_float(q.w << 16); v[7] = __uint_as_float(q.w & 0xffff0000u);
+}
+
+__device__ __forceinline__ uint4 pack_bf16x8(const float *v) {
+  return make_uint4(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]), pack_bf16x2(v[4], v[5]),
+                    pack_bf16x2(v[6], v[7]));
+}
+
+__device__ __forceinline__ uint4 ld_stream(const uint4 *p) {   // read-once data: skip L1
+  uint4 r;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w) : "l"(p));
+  return r;
+}
+
+__device__ __forceinline__ float sigmoidf_(float z) { return 1.0f / (1.0f + __expf(-z)); }
+
+inline int sm_count() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 148;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 148;
+  return n;
+}
+
+inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+inline size_t dtype_size(int dtype) { return dtype == MOE_F32 ? 4 : 2; }
+
+}  // namespace moe

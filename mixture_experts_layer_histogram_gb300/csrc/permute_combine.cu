@@ -1,0 +1,268 @@
+// Token permutation into the grouped layout, the weighted combine back to token order, and the
+// combine/routing backward. All three are HBM-bound row copies: one warp per token, 16-byte
+// vectors per lane, fp32 accumulation, the k row indices of a token held in lanes 0..k-1.
+//
+// "Scalable Pretraining of Large MoE LMs on Aurora", brief, section 核心方法: the generated indices
+// feed the grouped GEMM (permute) and the experts' outputs return to token order (combine); the
+// backward of both is part of the module's forward-backward pass (sections 为什么值得记录 / 关键结果).
+#include "common.cuh"
+
+namespace moe {
+
+constexpr int kRowThreads = 256;   // 8 warps, one token per warp per iteration
+constexpr int kUnroll = 4;         // 16-byte vectors in flight per lane
+
+template <typename T> struct Elem;
+template <> struct Elem<float> {
+  static constexpr int N = 4;
+  static __device__ __forceinline__ void unpack(const uint4 &q, float *v) {
+    v[0] = __uint_as_float(q.x); v[1] = __uint_as_float(q.y); v[2] = __uint_as_float(q.z); v[3] = __uint_as_float(q.w);
+  }
+  static __device__ __forceinline__ uint4 pack(const float *v) {
+    return make_uint4(__float_as_uint(v[0]), __float_as_uint(v[1]), __float_as_uint(v[2]), __float_as_uint(v[3]));
+  }
+};
+template <> struct Elem<__nv_bfloat16> {
+  static constexpr int N = 8;
+  static __device__ __forceinline__ void unpack(const uint4 &q, float *v) { unpack_bf16x8(q, v); }
+  static __device__ __forceinline__ uint4 pack(const float *v) { return pack_bf16x8(v); }
+};
+
+// Zero the padding rows of expert e: [tile_offsets[e]*BM + counts[e], tile_offsets[e+1]*BM).
+__device__ __forceinline__ void zero_padding_rows(uint4 *dst, int64_t row_vecs, int e, const int32_t *counts,
+                                                  const int32_t *tile_offsets, int BM, int64_t rows_max) {
+  int64_t start = (int64_t)tile_offsets[e] * BM + counts[e];
+  int64_t end = (int64_t)tile_offsets[e + 1] * BM;
+  if (end > rows_max) end = rows_max;
+  const uint4 z = make_uint4(0, 0, 0, 0);
+  for (int64_t i = start * row_vecs + threadIdx.x; i < end * row_vecs; i += blockDim.x) dst[i] = z;
+}
+
+__device__ __forceinline__ int load_row(const int32_t *row_of_slot, int64_t t, int k, int lane, int64_t rows_max) {
+  int r = -1;
+  if (lane < k) {
+    r = __ldg(row_of_slot + t * k + lane);
+    if (r < 0 || r >= rows_max) r = -1;
+  }
+  return r;
+}
+
+// ---------------------------------------------------------------------------------------------
+__global__ void __launch_bounds__(kRowThreads) permute_kernel(const uint4 *__restrict__ x, int64_t T, int64_t row_vecs,
+                                                              int k, const int32_t *__restrict__ row_of_slot,
+                                                              const int32_t *__restrict__ counts,
+                                                              const int32_t *__restrict__ tile_offsets, int BM,
+                                                              int64_t rows_max, int token_blocks,
+                                                              uint4 *__restrict__ xp) {
+  if ((int)blockIdx.x >= token_blocks) {
+    zero_padding_rows(xp, row_vecs, blockIdx.x - token_blocks, counts, tile_offsets, BM, rows_max);
+    return;
+  }
+  const int lane = threadIdx.x & 31;
+  const int64_t nw = (int64_t)token_blocks * (kRowThreads / 32);
+  for (int64_t t = (int64_t)blockIdx.x * (kRowThreads / 32) + (threadIdx.x >> 5); t < T; t += nw) {
+    const int myrow = load_row(row_of_slot, t, k, lane, rows_max);
+    const uint4 *src = x + t * row_vecs;
+    for (int64_t v0 = 0; v0 < row_vecs; v0 += 32 * kUnroll) {
+      uint4 buf[kUnroll];
+#pragma unroll
+      for (int u = 0; u < kUnroll; ++u) {
+        int64_t v = v0 + u * 32 + lane;
+        if (v < row_vecs) buf[u] = ld_stream(src + v);
+      }
+      for (int j = 0; j < k; ++j) {
+        int r = __shfl_sync(0xffffffffu, myrow, j);
+        if (r < 0) continue;
+        uint4 *dst = xp + (int64_t)r * row_vecs;
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) {
+          int64_t v = v0 + u * 32 + lane;
+          if (v < row_vecs) dst[v] = buf[u];
+        }
+      }
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------------------------
+template <typename T, bool WEIGHTED>
+__global__ void __launch_bounds__(kRowThreads) combine_kernel(const uint4 *__restrict__ y, const float *__restrict__ w,
+                                                              const int32_t *__restrict__ row_of_slot, int64_t Tn,
+                                                              int64_t row_vecs, int k, int64_t rows_max,
+                                                              uint4 *__restrict__ out) {
+  constexpr int N = Elem<T>::N;
+  const int lane = threadIdx.x & 31;
+  const int64_t nw = (int64_t)gridDim.x * (kRowThreads / 32);
+  for (int64_t t = (int64_t)blockIdx.x * (kRowThreads / 32) + (threadIdx.x >> 5); t < Tn; t += nw) {
+    const int myrow = load_row(row_of_slot, t, k, lane, rows_max);
+    const float myw = (WEIGHTED && lane < k) ? __ldg(w + t * k + lane) : 1.0f;
+    for (int64_t v = lane; v < row_vecs; v += 32) {
+      float acc[N];
+#pragma unroll
+      for (int i = 0; i < N; ++i) acc[i] = 0.0f;
+      for (int j = 0; j < k; ++j) {
+        int r = __shfl_sync(0xffffffffu, myrow, j);
+        float wj = __shfl_sync(0xffffffffu, myw, j);
+        if (r < 0) continue;
+        float val[N];
+        Elem<T>::unpack(ld_stream(y + (int64_t)r * row_vecs + v), val);
+#pragma unroll
+        for (int i = 0; i < N; ++i) acc[i] = WEIGHTED ? fmaf(wj, val[i], acc[i]) : acc[i] + val[i];
+      }
+      out[t * row_vecs + v] = Elem<T>::pack(acc);
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------------------------
+template <typename T>
+__global__ void __launch_bounds__(kRowThreads) combine_bwd_kernel(
+    const uint4 *__restrict__ g, const uint4 *__restrict__ y, const float *__restrict__ w,
+    const int32_t *__restrict__ topk_idx, const int32_t *__restrict__ row_of_slot, const int32_t *__restrict__ counts,
+    const int32_t *__restrict__ tile_offsets, int BM, int64_t Tn, int64_t row_vecs, int k, int E, int64_t rows_max,
+    int token_blocks, uint4 *__restrict__ dy, float *__restrict__ d_topk_w, float *__restrict__ d_logits) {
+  if ((int)blockIdx.x >= token_blocks) {
+    zero_padding_rows(dy, row_vecs, blockIdx.x - token_blocks, counts, tile_offsets, BM, rows_max);
+    return;
+  }
+  constexpr int N = Elem<T>::N;
+  const int lane = threadIdx.x & 31;
+  const int64_t nw = (int64_t)token_blocks * (kRowThreads / 32);
+  for (int64_t t = (int64_t)blockIdx.x * (kRowThreads / 32) + (threadIdx.x >> 5); t < Tn; t += nw) {
+    const int myrow = load_row(row_of_slot, t, k, lane, rows_max);
+    const float myw = lane < k ? __ldg(w + t * k + lane) : 0.0f;
+    const int mye = lane < k ? __ldg(topk_idx + t * k + lane) : -1;
+    float part[MOE_MAX_TOPK];
+#pragma unroll
+    for (int j = 0; j < MOE_MAX_TOPK; ++j) part[j] = 0.0f;
+    for (int64_t v = lane; v < row_vecs; v += 32) {
+      float gv[N];
+      Elem<T>::unpack(ld_stream(g + t * row_vecs + v), gv);
+#pragma unroll
+      for (int j = 0; j < MOE_MAX_TOPK; ++j) {
+        if (j >= k) break;
+        int r = __shfl_sync(0xffffffffu, myrow, j);
+        float wj = __shfl_sync(0xffffffffu, myw, j);
+        if (r < 0) continue;
+        float yv[N], o[N];
+        Elem<T>::unpack(ld_stream(y + (int64_t)r * row_vecs + v), yv);
+        float s = 0.0f;
+#pragma unroll
+        for (int i = 0; i < N; ++i) {
+          s = fmaf(gv[i], yv[i], s);
+          o[i] = wj * gv[i];
+        }
+        part[j] += s;
+        dy[(int64_t)r * row_vecs + v] = Elem<T>::pack(o);
+      }
+    }
+    // d_topk_w[t, j] = <g, y_j>: reduce each partial over the warp; lane j keeps slot j
+    float dw = 0.0f;
+#pragma unroll
+    for (int j = 0; j < MOE_MAX_TOPK; ++j) {
+      if (j >= k) break;
+      float s = part[j];
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
+      if (lane == j) dw = s;
+    }
+    float sw = lane < k ? myw * dw : 0.0f;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) sw += __shfl_xor_sync(0xffffffffu, sw, off);
+    const float dl = myw * (dw - sw);
+    if (lane < k) d_topk_w[t * k + lane] = dw;
+    for (int e0 = 0; e0 < E; e0 += 32) {
+      int e = e0 + lane;
+      float val = 0.0f;
+      for (int j = 0; j < k; ++j) {
+        int ej = __shfl_sync(0xffffffffu, mye, j);
+        float dj = __shfl_sync(0xffffffffu, dl, j);
+        if (ej == e) val = dj;
+      }
+      if (e < E) d_logits[t * E + e] = val;
+    }
+  }
+}
+
+static int row_blocks(int64_t T) {
+  int64_t b = (T + (kRowThreads / 32) - 1) / (kRowThreads / 32);
+  int64_t cap = (int64_t)sm_count() * 8;
+  if (b > cap) b = cap;
+  if (b < 1) b = 1;
+  return (int)b;
+}
+
+}  // namespace moe
+
+using namespace moe;
+
+static bool valid_dtype(int dtype) { return dtype == MOE_F32 || dtype == MOE_BF16; }
+
+extern "C" int moe_permute(const void *x, int dtype, int T, int d, int k, int E, const int32_t *row_of_slot,
+                           const int32_t *counts, const int32_t *tile_offsets, int64_t rows_max, void *x_perm,
+                           moe_stream_t stream) {
+  if (!valid_dtype(dtype) || T < 0 || d < 1 || k < 1 || k > MOE_MAX_TOPK || E < 1 || E > MOE_MAX_EXPERTS)
+    return MOE_ERR_INVALID_ARG;
+  const size_t row_bytes = (size_t)d * dtype_size(dtype);
+  if (row_bytes % 16) return MOE_ERR_UNSUPPORTED;
+  if (rows_max < moe_grouped_rows_max(T, k, E)) return MOE_ERR_INVALID_ARG;
+  if (!x_perm || !counts || !tile_offsets || (T > 0 && (!x || !row_of_slot))) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(x_perm)) return MOE_ERR_INVALID_ARG;
+  const int tb = row_blocks(T);
+  permute_kernel<<<tb + E, kRowThreads, 0, (cudaStream_t)stream>>>(
+      (const uint4 *)x, T, (int64_t)(row_bytes / 16), k, row_of_slot, counts, tile_offsets, MOE_GROUP_ROWS, rows_max,
+      tb, (uint4 *)x_perm);
+  MOE_CHECK_LAUNCH();
+  return MOE_OK;
+}
+
+extern "C" int moe_combine_fwd(const void *y_perm, const float *topk_w, const int32_t *row_of_slot, int T, int d,
+                               int k, int64_t rows_max, int dtype, void *out, moe_stream_t stream) {
+  if (!valid_dtype(dtype) || T < 0 || d < 1 || k < 1 || k > MOE_MAX_TOPK || rows_max < 0) return MOE_ERR_INVALID_ARG;
+  const size_t row_bytes = (size_t)d * dtype_size(dtype);
+  if (row_bytes % 16) return MOE_ERR_UNSUPPORTED;
+  if (T == 0) return MOE_OK;
+  if (!y_perm || !row_of_slot || !out || !aligned16(y_perm) || !aligned16(out)) return MOE_ERR_INVALID_ARG;
+  const int64_t rv = (int64_t)(row_bytes / 16);
+  const int nb = row_blocks(T);
+  cudaStream_t s = (cudaStream_t)stream;
+  const uint4 *y = (const uint4 *)y_perm;
+  uint4 *o = (uint4 *)out;
+  if (dtype == MOE_BF16) {
+    if (topk_w) combine_kernel<__nv_bfloat16, true><<<nb, kRowThreads, 0, s>>>(y, topk_w, row_of_slot, T, rv, k, rows_max, o);
+    else combine_kernel<__nv_bfloat16, false><<<nb, kRowThreads, 0, s>>>(y, topk_w, row_of_slot, T, rv, k, rows_max, o);
+  } else {
+    if (topk_w) combine_kernel<float, true><<<nb, kRowThreads, 0, s>>>(y, topk_w, row_of_slot, T, rv, k, rows_max, o);
+    else combine_kernel<float, false><<<nb, kRowThreads, 0, s>>>(y, topk_w, row_of_slot, T, rv, k, rows_max, o);
+  }
+  MOE_CHECK_LAUNCH();
+  return MOE_OK;
+}
+
+extern "C" int moe_combine_bwd(const void *grad_out, const void *y_perm, const float *topk_w, const int32_t *topk_idx,
+                               const int32_t *row_of_slot, const int32_t *counts, const int32_t *tile_offsets, int T,
+                               int d, int k, int E, int64_t rows_max, int dtype, void *dy_perm, float *d_topk_w,
+                               float *d_logits, moe_stream_t stream) {
+  if (!valid_dtype(dtype) || T < 0 || d < 1 || k < 1 || k > MOE_MAX_TOPK || E < 1 || E > MOE_MAX_EXPERTS || k > E)
+    return MOE_ERR_INVALID_ARG;
+  const size_t row_bytes = (size_t)d * dtype_size(dtype);
+  if (row_bytes % 16) return MOE_ERR_UNSUPPORTED;
+  if (rows_max < moe_grouped_rows_max(T, k, E)) return MOE_ERR_INVALID_ARG;
+  if (!dy_perm || !counts || !tile_offsets || !aligned16(dy_perm)) return MOE_ERR_INVALID_ARG;
+  if (T > 0 && (!grad_out || !y_perm || !topk_w || !topk_idx || !row_of_slot || !d_topk_w || !d_logits ||
+                !aligned16(grad_out) || !aligned16(y_perm)))
+    return MOE_ERR_INVALID_ARG;
+  const int64_t rv = (int64_t)(row_bytes / 16);
+  const int tb = row_blocks(T);
+  cudaStream_t s = (cudaStream_t)stream;
+  if (dtype == MOE_BF16)
+    combine_bwd_kernel<__nv_bfloat16><<<tb + E, kRowThreads, 0, s>>>(
+        (const uint4 *)grad_out, (const uint4 *)y_perm, topk_w, topk_idx, row_of_slot, counts, tile_offsets,
+        MOE_GROUP_ROWS, T, rv, k, E, rows_max, tb, (uint4 *)dy_perm, d_topk_w, d_logits);
+  else
+    combine_bwd_kernel<float><<<tb + E, kRowThreads, 0, s>>>(
+        (const uint4 *)grad_out, (const uint4 *)y_perm, topk_w, topk_idx, row_of_slot, counts, tile_offsets,
+        MOE_GROUP_ROWS, T, rv, k, E, rows_max, tb, (uint4 *)dy_perm, d_topk_w, d_logits);
+  MOE_CHECK_LAUNCH();
+  return MOE_OK;
+}

@@ -1,0 +1,336 @@
+// Routing (top-k + renormalised softmax), token counting and index generation.
+//
+// "Scalable Pretraining of Large MoE LMs on Aurora", brief, section 核心方法: FastSparseMoE counts
+// the tokens of each expert and generates their indices with GPU kernels before the grouped GEMM.
+// Here that is a stable counting sort of the T*k routing slots by expert id:
+//   count kernel : warp-aggregated (match.any) shared-memory histograms, one global atomic per
+//                  (block, expert); the last block to finish scans counts into offsets and tile offsets.
+//   index kernel : every block ranks its chunk of slots stably (match.any + per-warp counts), then
+//                  finds, per expert, how many earlier slots went to that expert with a decoupled
+//                  look-back over the preceding blocks (one 64-bit flag|value word per block and
+//                  expert), and scatters row_of_slot / token_of_row.
+#include "common.cuh"
+
+namespace moe {
+
+constexpr int kRouteThreads = 256;
+constexpr int kIdxThreads = 256;                 // 8 warps
+constexpr int kIdxItems = 4;                     // slots per thread
+constexpr int kIdxChunk = kIdxThreads * kIdxItems;
+
+// look-back word: flag in the high 32 bits, value in the low 32 bits
+constexpr uint64_t kFlagAggregate = 1ull << 32;
+constexpr uint64_t kFlagPrefix = 2ull << 32;
+
+// ---------------------------------------------------------------------------------------------
+// top-k routing: one warp per token; lane l owns experts l, l+32, ...
+template <int EPL>
+__global__ void __launch_bounds__(kRouteThreads) route_topk_kernel(const float *__restrict__ logits, int T, int E,
+                                                                   int k, int32_t *__restrict__ topk_idx,
+                                                                   float *__restrict__ topk_w) {
+  const int lane = threadIdx.x & 31;
+  const int nwarps = gridDim.x * (kRouteThreads / 32);
+  for (int t = blockIdx.x * (kRouteThreads / 32) + (threadIdx.x >> 5); t < T; t += nwarps) {
+    float v[EPL];
+#pragma unroll
+    for (int i = 0; i < EPL; ++i) {
+      int e = lane + 32 * i;
+      v[i] = e < E ? __ldg(logits + (size_t)t * E + e) : 0.0f;
+    }
+    uint32_t taken = 0;
+    int my_e = 0;
+    float my_v = 0.0f;
+    for (int j = 0; j < k; ++j) {
+      float bv = 0.0f;
+      int be = 0x7fffffff;   // "no candidate"
+#pragma unroll
+      for (int i = 0; i < EPL; ++i) {
+        int e = lane + 32 * i;
+        bool ok = e < E && !((taken >> i) & 1u);
+        if (ok && (be == 0x7fffffff || v[i] > bv)) { bv = v[i]; be = e; }   // ascending e: ties keep lower id
+      }
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) {
+        float ov = __shfl_xor_sync(0xffffffffu, bv, off);
+        int oe = __shfl_xor_sync(0xffffffffu, be, off);
+        bool take = (oe != 0x7fffffff) && (be == 0x7fffffff || ov > bv || (ov == bv && oe < be));
+        if (take) { bv = ov; be = oe; }
+      }
+      if ((be & 31) == lane) taken |= 1u << (be >> 5);
+      if (lane == j) { my_e = be; my_v = bv; }
+    }
+    const float m = __shfl_sync(0xffffffffu, my_v, 0);   // largest selected logit
+    float ex = lane < k ? expf(my_v - m) : 0.0f;
+    float s = ex;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
+    if (lane < k) {
+      topk_idx[(size_t)t * k + lane] = my_e;
+      topk_w[(size_t)t * k + lane] = ex / s;
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------------------------
+// count kernel
+struct IndexWs {
+  WsHeader hdr;   // tickets[0]: count blocks done, tickets[1]: index block ticket
+};
+
+__device__ __forceinline__ int slot_key(const int32_t *__restrict__ idx, int64_t s, int64_t n, int E, WsHeader *hdr) {
+  if (s >= n) return -1;
+  int e = __ldg(idx + s);
+  if ((unsigned)e >= (unsigned)E) {
+    report(hdr, MOE_ERR_BAD_INDEX, (int)s);
+    return -1;
+  }
+  return e;
+}
+
+__global__ void __launch_bounds__(kIdxThreads) count_kernel(const int32_t *__restrict__ idx, int64_t n, int E, int BM,
+                                                            WsHeader *hdr, int32_t *__restrict__ acc, int32_t *hook,
+                                                            uint64_t *__restrict__ lookback, int32_t *__restrict__ counts,
+                                                            int32_t *__restrict__ offsets,
+                                                            int32_t *__restrict__ tile_offsets) {
+  __shared__ int hist[MOE_MAX_EXPERTS];
+  __shared__ bool is_last;
+  const int tid = threadIdx.x, lane = tid & 31;
+  for (int e = tid; e < E; e += kIdxThreads) {
+    hist[e] = 0;
+    lookback[(size_t)blockIdx.x * E + e] = 0;   // reset this block's look-back words for the index kernel
+  }
+  __syncthreads();
+  const int64_t base = (int64_t)blockIdx.x * kIdxChunk;
+#pragma unroll
+  for (int i = 0; i < kIdxItems; ++i) {
+    int key = slot_key(idx, base + i * kIdxThreads + tid, n, E, hdr);
+    unsigned peers = __match_any_sync(0xffffffffu, key);
+    if (key >= 0 && lane == __ffs(peers) - 1) atomicAdd(&hist[key], __popc(peers));
+  }
+  __syncthreads();
+  for (int e = tid; e < E; e += kIdxThreads)
+    if (hist[e]) atomicAdd(acc + e, hist[e]);
+  __threadfence();
+  __syncthreads();
+  if (tid == 0) is_last = atomicAdd(&hdr->tickets[0], 1u) == gridDim.x - 1;
+  __syncthreads();
+  if (!is_last) return;
+  __threadfence();
+  if (tid == 0) {   // arm (or disarm) the look-back fault hook for the index kernel, then clear it
+    hdr->armed = *hook;
+    *hook = 0;
+  }
+  // last block: exclusive scans of counts and of ceil(counts / BM); warp 0, 8 experts per lane
+  if (tid < 32) {
+    int c[8], tl[8], sc = 0, st = 0;
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      int e = lane * 8 + q;
+      c[q] = e < E ? atomicAdd(acc + e, 0) : 0;
+      tl[q] = (c[q] + BM - 1) / BM;
+      sc += c[q];
+      st += tl[q];
+    }
+    int ic = sc, it = st;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      int a = __shfl_up_sync(0xffffffffu, ic, off), b = __shfl_up_sync(0xffffffffu, it, off);
+      if (lane >= off) { ic += a; it += b; }
+    }
+    int rc = ic - sc, rt = it - st;   // exclusive prefix of this lane's first expert
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      int e = lane * 8 + q;
+      if (e < E) {
+        counts[e] = c[q];
+        offsets[e] = rc;
+        tile_offsets[e] = rt;
+      }
+      rc += c[q];
+      rt += tl[q];
+    }
+    if (lane == 31) {
+      offsets[E] = ic;
+      tile_offsets[E] = it;
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------------------------
+// index kernel: stable ranks + per-expert decoupled look-back + scatter
+__global__ void __launch_bounds__(kIdxThreads) index_kernel(const int32_t *__restrict__ idx, int64_t n, int k, int E,
+                                                            int BM, WsHeader *hdr, uint64_t *__restrict__ lookback,
+                                                            const int32_t *__restrict__ counts,
+                                                            const int32_t *__restrict__ tile_offsets,
+                                                            int32_t *__restrict__ row_of_slot,
+                                                            int32_t *__restrict__ token_of_row) {
+  __shared__ int warp_cnt[kIdxThreads / 32][MOE_MAX_EXPERTS];
+  __shared__ int run[MOE_MAX_EXPERTS];
+  __shared__ int excl[MOE_MAX_EXPERTS];
+  __shared__ int row_base[MOE_MAX_EXPERTS];
+  __shared__ int bid_s;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  if (tid == 0) bid_s = (int)atomicAdd(&hdr->tickets[1], 1u);   // dynamic block id: predecessors already run
+  for (int i = tid; i < (kIdxThreads / 32) * MOE_MAX_EXPERTS; i += kIdxThreads) (&warp_cnt[0][0])[i] = 0;
+  for (int e = tid; e < E; e += kIdxThreads) {
+    run[e] = 0;
+    row_base[e] = tile_offsets[e] * BM;
+  }
+  __syncthreads();
+  const int b = bid_s;
+  const int64_t base = (int64_t)b * kIdxChunk;
+  const unsigned lt_mask = (1u << lane) - 1u;
+  int key[kIdxItems], rank[kIdxItems];
+#pragma unroll
+  for (int i = 0; i < kIdxItems; ++i) {
+    key[i] = slot_key(idx, base + i * kIdxThreads + tid, n, E, nullptr);
+    unsigned peers = __match_any_sync(0xffffffffu, key[i]);
+    int r_in_warp = __popc(peers & lt_mask);
+    bool leader = key[i] >= 0 && lane == __ffs(peers) - 1;
+    if (leader) warp_cnt[warp][key[i]] = __popc(peers);
+    __syncthreads();
+    for (int e = tid; e < E; e += kIdxThreads) {   // exclusive scan over warps, on top of earlier rounds
+      int r = run[e];
+#pragma unroll
+      for (int w = 0; w < kIdxThreads / 32; ++w) {
+        int c = warp_cnt[w][e];
+        warp_cnt[w][e] = r;
+        r += c;
+      }
+      run[e] = r;
+    }
+    __syncthreads();
+    rank[i] = key[i] >= 0 ? warp_cnt[warp][key[i]] + r_in_warp : 0;
+    __syncthreads();
+    for (int j = tid; j < (kIdxThreads / 32) * MOE_MAX_EXPERTS; j += kIdxThreads) (&warp_cnt[0][0])[j] = 0;
+    __syncthreads();
+  }
+  // publish this block's per-expert aggregate, then look back over predecessors
+  const bool withhold = (b == hdr->armed - 1);
+  for (int e = tid; e < E; e += kIdxThreads) {
+    const uint32_t agg = (uint32_t)run[e];
+    volatile uint64_t *mine = lookback + (size_t)b * E + e;
+    if (b == 0) {
+      if (!withhold) *mine = kFlagPrefix | agg;
+      excl[e] = 0;
+      continue;
+    }
+    if (!withhold) *mine = kFlagAggregate | agg;
+    uint32_t sum = 0;
+    int p = b - 1;
+    uint64_t t0 = 0;
+    while (p >= 0) {
+      uint64_t v = *(volatile uint64_t *)(lookback + (size_t)p * E + e);
+      uint64_t flag = v & 0xffffffff00000000ull;
+      if (flag == 0) {
+        uint64_t now = global_ns();
+        if (t0 == 0) t0 = now;
+        if (now - t0 > kWaitLimitNs) {
+          report(hdr, MOE_ERR_DEVICE_TIMEOUT, b);
+          break;
+        }
+        __nanosleep(64);
+        continue;
+      }
+      sum += (uint32_t)v;
+      if (flag == kFlagPrefix) break;
+      --p;
+    }
+    excl[e] = (int)sum;
+    if (!withhold) *mine = kFlagPrefix | (sum + agg);
+  }
+  __syncthreads();
+#pragma unroll
+  for (int i = 0; i < kIdxItems; ++i) {
+    int64_t s = base + i * kIdxThreads + tid;
+    if (s >= n) continue;
+    if (key[i] < 0) {
+      row_of_slot[s] = -1;
+      continue;
+    }
+    int row = row_base[key[i]] + excl[key[i]] + rank[i];
+    row_of_slot[s] = row;
+    token_of_row[row] = (int)(s / k);
+  }
+  // padding rows of the grouped layout
+  for (int e = blockIdx.x; e < E; e += gridDim.x) {
+    int start = tile_offsets[e] * BM + counts[e], end = tile_offsets[e + 1] * BM;
+    for (int r = start + tid; r < end; r += kIdxThreads) token_of_row[r] = -1;
+  }
+}
+
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" int moe_route_topk(const float *logits, int T, int E, int k, int32_t *topk_idx, float *topk_w,
+                              moe_stream_t stream) {
+  if (T < 0 || E < 1 || E > MOE_MAX_EXPERTS || k < 1 || k > E || k > MOE_MAX_TOPK) return MOE_ERR_INVALID_ARG;
+  if (T == 0) return MOE_OK;
+  if (!logits || !topk_idx || !topk_w) return MOE_ERR_INVALID_ARG;
+  const int warps = kRouteThreads / 32;
+  int blocks = (int)(((int64_t)T + warps - 1) / warps);
+  const int cap = sm_count() * 16;
+  if (blocks > cap) blocks = cap;
+  cudaStream_t s = (cudaStream_t)stream;
+  if (E <= 32) route_topk_kernel<1><<<blocks, kRouteThreads, 0, s>>>(logits, T, E, k, topk_idx, topk_w);
+  else if (E <= 64) route_topk_kernel<2><<<blocks, kRouteThreads, 0, s>>>(logits, T, E, k, topk_idx, topk_w);
+  else if (E <= 128) route_topk_kernel<4><<<blocks, kRouteThreads, 0, s>>>(logits, T, E, k, topk_idx, topk_w);
+  else route_topk_kernel<8><<<blocks, kRouteThreads, 0, s>>>(logits, T, E, k, topk_idx, topk_w);
+  MOE_CHECK_LAUNCH();
+  return MOE_OK;
+}
+
+extern "C" int64_t moe_grouped_rows_max(int T, int k, int E) {
+  if (T < 0 || k < 1 || E < 1) return -1;
+  int64_t r = (int64_t)T * k + (int64_t)E * (MOE_GROUP_ROWS - 1);
+  return (r + MOE_GROUP_ROWS - 1) / MOE_GROUP_ROWS * MOE_GROUP_ROWS;
+}
+
+static int64_t index_blocks(int T, int k) { return ((int64_t)T * k + kIdxChunk - 1) / kIdxChunk; }
+
+// layout: [IndexWs header][acc: E int32, padded to 256 B][fault hook int32, padded to 256 B]
+//         [lookback: blocks * E uint64]
+static size_t acc_bytes(int E) { return ((size_t)E * 4 + 255) / 256 * 256; }
+constexpr size_t kHookBytes = 256;
+
+extern "C" size_t moe_count_index_workspace_size(int T, int k, int E) {
+  if (T < 0 || k < 1 || E < 1) return 0;
+  int64_t nb = index_blocks(T, k);
+  if (nb < 1) nb = 1;
+  return sizeof(IndexWs) + acc_bytes(E) + kHookBytes + (size_t)nb * E * sizeof(uint64_t);
+}
+
+extern "C" int moe_count_index(const int32_t *topk_idx, int T, int k, int E, int32_t *counts, int32_t *offsets,
+                               int32_t *tile_offsets, int32_t *row_of_slot, int32_t *token_of_row, void *ws,
+                               size_t ws_bytes, moe_stream_t stream) {
+  if (T < 0 || E < 1 || E > MOE_MAX_EXPERTS || k < 1 || k > MOE_MAX_TOPK) return MOE_ERR_INVALID_ARG;
+  if ((int64_t)T * k >= (int64_t)1 << 31) return MOE_ERR_UNSUPPORTED;
+  if (!counts || !offsets || !tile_offsets || !token_of_row || !ws) return MOE_ERR_INVALID_ARG;
+  if (T > 0 && (!topk_idx || !row_of_slot)) return MOE_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(ws) & 255) != 0) return MOE_ERR_INVALID_ARG;
+  if (ws_bytes < moe_count_index_workspace_size(T, k, E)) return MOE_ERR_INVALID_ARG;
+  cudaStream_t s = (cudaStream_t)stream;
+  char *w = static_cast<char *>(ws);
+  IndexWs *iw = reinterpret_cast<IndexWs *>(w);
+  int32_t *acc = reinterpret_cast<int32_t *>(w + sizeof(IndexWs));
+  uint64_t *lookback = reinterpret_cast<uint64_t *>(w + sizeof(IndexWs) + acc_bytes(E) + kHookBytes);
+  // One memset resets the status word, the tickets and the histogram accumulator; the fault hook
+  // lives after them and is consumed (read and cleared) by the count kernel's last block.
+  MOE_TRY_CUDA(cudaMemsetAsync(w, 0, sizeof(IndexWs) + acc_bytes(E), s));
+  int32_t *hook = reinterpret_cast<int32_t *>(w + sizeof(IndexWs) + acc_bytes(E));
+  const int64_t n = (int64_t)T * k;
+  const int nb = (int)(n > 0 ? index_blocks(T, k) : 1);
+  count_kernel<<<nb, kIdxThreads, 0, s>>>(topk_idx, n, E, MOE_GROUP_ROWS, &iw->hdr, acc, hook, lookback, counts,
+                                          offsets, tile_offsets);
+  MOE_CHECK_LAUNCH();
+  index_kernel<<<nb, kIdxThreads, 0, s>>>(topk_idx, n, k, E, MOE_GROUP_ROWS, &iw->hdr, lookback, counts,
+                                          tile_offsets, row_of_slot, token_of_row);
+  MOE_CHECK_LAUNCH();
+  return MOE_OK;
+}
+
+extern "C" size_t moe_count_index_hook_offset(int E) {
+  if (E < 1) return 0;
+  return sizeof(IndexWs) + acc_bytes(E);
+}

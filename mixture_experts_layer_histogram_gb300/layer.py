@@ -1,0 +1,91 @@
+"""One MoE layer's expert computation on one GPU: resident buffers and the call sequence.
+
+Forward (one stream, no host synchronisation):
+  moe_route_topk   logits [T,E]        -> topk_idx [T,k], topk_w [T,k]
+  moe_count_index  topk_idx            -> counts, offsets, tile_offsets, row_of_slot, token_of_row
+  moe_permute      x [T,d]             -> x_perm [rows_max,d]
+  moe_grouped_ffn_fwd                  -> ab [rows_max,2f], h [rows_max,f], y_perm [rows_max,d]
+  moe_combine_fwd  y_perm, topk_w      -> out [T,d]
+Backward:
+  moe_combine_bwd  grad_out            -> dy_perm, d_topk_w [T,k], d_logits [T,E]
+  moe_grouped_ffn_bwd                  -> dab, dx_perm, dw_gate_up [E,2f,d], dw_down [E,d,f]
+  moe_combine_fwd  dx_perm, w = NULL   -> dx [T,d]      (backward of the permutation)
+
+Every step runs in libmoe's kernels; this module only allocates buffers (PyTorch device memory)
+and calls the C ABI in order.
+"""
+from __future__ import annotations
+
+import torch
+
+from . import _lib as L
+
+
+class MoELayer:
+    """Buffers of one layer pass, allocated once and reused every step (no allocation per step)."""
+
+    def __init__(self, T, d, E, k, f, dtype=torch.bfloat16, device="cuda", backward=True):
+        if not torch.cuda.is_available():
+            raise RuntimeError("MoELayer needs a CUDA device")
+        self.T, self.d, self.E, self.k, self.f = T, d, E, k, f
+        self.dtype = dtype
+        self.device = torch.device(device)
+        self.rows_max = L.moe_grouped_rows_max(T, k, E)
+        R = self.rows_max
+        i32 = dict(dtype=torch.int32, device=self.device)
+        act = dict(dtype=dtype, device=self.device)
+        self.topk_idx = torch.empty((T, k), **i32)
+        self.topk_w = torch.empty((T, k), dtype=torch.float32, device=self.device)
+        self.counts = torch.empty(E, **i32)
+        self.offsets = torch.empty(E + 1, **i32)
+        self.tile_offsets = torch.empty(E + 1, **i32)
+        self.row_of_slot = torch.empty(T * k, **i32)
+        self.token_of_row = torch.empty(R, **i32)
+        self.ws_index = torch.zeros(L.moe_count_index_workspace_size(T, k, E), dtype=torch.uint8, device=self.device)
+        self.ws_ffn = torch.zeros(L.moe_grouped_ffn_workspace_size(E, d, f, R, L.dtype_code(dtype), backward),
+                                  dtype=torch.uint8, device=self.device)
+        self.x_perm = torch.empty((R, d), **act)
+        self.ab = torch.empty((R, 2 * f), **act)
+        self.h = torch.empty((R, f), **act)
+        self.y_perm = torch.empty((R, d), **act)
+        self.out = torch.empty((T, d), **act)
+        self.backward_enabled = backward
+        if backward:
+            self.dy_perm = torch.empty((R, d), **act)
+            self.dab = torch.empty((R, 2 * f), **act)
+            self.dx_perm = torch.empty((R, d), **act)
+            self.dx = torch.empty((T, d), **act)
+            self.d_topk_w = torch.empty((T, k), dtype=torch.float32, device=self.device)
+            self.d_logits = torch.empty((T, E), dtype=torch.float32, device=self.device)
+            self.dw_gate_up = torch.empty((E, 2 * f, d), **act)
+            self.dw_down = torch.empty((E, d, f), **act)
+
+    def forward(self, x, logits, w_gate_up, w_down, stream=None):
+        L.moe_route_topk(logits, self.k, self.topk_idx, self.topk_w, stream)
+        L.moe_count_index(self.topk_idx, self.E, self.counts, self.offsets, self.tile_offsets, self.row_of_slot,
+                          self.token_of_row, self.ws_index, stream)
+        L.moe_permute(x, self.k, self.E, self.row_of_slot, self.counts, self.tile_offsets, self.x_perm, stream)
+        L.moe_grouped_ffn_fwd(self.x_perm, w_gate_up, w_down, self.tile_offsets, self.ab, self.h, self.y_perm,
+                              self.ws_ffn, stream)
+        L.moe_combine_fwd(self.y_perm, self.topk_w, self.row_of_slot, self.T, self.k, self.out, stream)
+        return self.out
+
+    def backward(self, grad_out, w_gate_up, w_down, stream=None):
+        if not self.backward_enabled:
+            raise RuntimeError("layer was built without backward buffers")
+        L.moe_combine_bwd(grad_out, self.y_perm, self.topk_w, self.topk_idx, self.row_of_slot, self.counts,
+                          self.tile_offsets, self.E, self.dy_perm, self.d_topk_w, self.d_logits, stream)
+        L.moe_grouped_ffn_bwd(self.dy_perm, self.x_perm, self.ab, self.h, w_gate_up, w_down, self.tile_offsets,
+                              self.dab, self.dx_perm, self.dw_gate_up, self.dw_down, self.ws_ffn, stream)
+        L.moe_combine_fwd(self.dx_perm, None, self.row_of_slot, self.T, self.k, self.dx, stream)
+        return dict(dx=self.dx, d_logits=self.d_logits, d_topk_w=self.d_topk_w, dw_gate_up=self.dw_gate_up,
+                    dw_down=self.dw_down)
+
+    def status(self, stream=None):
+        """Device status words (synchronises): (count_index, grouped_ffn)."""
+        return L.moe_read_status(self.ws_index, stream), L.moe_read_status(self.ws_ffn, stream)
+
+    # kernels launched per pass, for the bench's launch count
+    def launches(self, backward=True):
+        fwd = 1 + 2 + 1 + 2 + 1
+        return fwd + (1 + 4 + 1 if backward else 0)
