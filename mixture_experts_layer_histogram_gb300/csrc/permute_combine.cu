@@ -96,20 +96,23 @@ __global__ void __launch_bounds__(kRowThreads) combine_kernel(const uint4 *__res
   for (int64_t t = (int64_t)blockIdx.x * (kRowThreads / 32) + (threadIdx.x >> 5); t < Tn; t += nw) {
     const int myrow = load_row(row_of_slot, t, k, lane, rows_max);
     const float myw = (WEIGHTED && lane < k) ? __ldg(w + t * k + lane) : 1.0f;
-    for (int64_t v = lane; v < row_vecs; v += 32) {
+    // warp-uniform loop: every lane reaches every shuffle; loads and stores are predicated
+    for (int64_t v0 = 0; v0 < row_vecs; v0 += 32) {
+      const int64_t v = v0 + lane;
+      const bool act = v < row_vecs;
       float acc[N];
 #pragma unroll
       for (int i = 0; i < N; ++i) acc[i] = 0.0f;
       for (int j = 0; j < k; ++j) {
         int r = __shfl_sync(0xffffffffu, myrow, j);
         float wj = __shfl_sync(0xffffffffu, myw, j);
-        if (r < 0) continue;
+        if (r < 0 || !act) continue;
         float val[N];
         Elem<T>::unpack(ld_stream(y + (int64_t)r * row_vecs + v), val);
 #pragma unroll
         for (int i = 0; i < N; ++i) acc[i] = WEIGHTED ? fmaf(wj, val[i], acc[i]) : acc[i] + val[i];
       }
-      out[t * row_vecs + v] = Elem<T>::pack(acc);
+      if (act) out[t * row_vecs + v] = Elem<T>::pack(acc);
     }
   }
 }
@@ -135,15 +138,18 @@ __global__ void __launch_bounds__(kRowThreads) combine_bwd_kernel(
     float part[MOE_MAX_TOPK];
 #pragma unroll
     for (int j = 0; j < MOE_MAX_TOPK; ++j) part[j] = 0.0f;
-    for (int64_t v = lane; v < row_vecs; v += 32) {
+    // warp-uniform loop: every lane reaches every shuffle; loads and stores are predicated
+    for (int64_t v0 = 0; v0 < row_vecs; v0 += 32) {
+      const int64_t v = v0 + lane;
+      const bool act = v < row_vecs;
       float gv[N];
-      Elem<T>::unpack(ld_stream(g + t * row_vecs + v), gv);
+      if (act) Elem<T>::unpack(ld_stream(g + t * row_vecs + v), gv);
 #pragma unroll
       for (int j = 0; j < MOE_MAX_TOPK; ++j) {
         if (j >= k) break;
         int r = __shfl_sync(0xffffffffu, myrow, j);
         float wj = __shfl_sync(0xffffffffu, myw, j);
-        if (r < 0) continue;
+        if (r < 0 || !act) continue;
         float yv[N], o[N];
         Elem<T>::unpack(ld_stream(y + (int64_t)r * row_vecs + v), yv);
         float s = 0.0f;
