@@ -83,7 +83,7 @@ def test_permute_is_exact_copy_and_padding_is_zero():
     layer, _, inp = _run(w)
     xp = layer.x_perm.cpu()
     ros = layer.row_of_slot.cpu().long()
-    assert torch.equal(xp[ros], inp["x"].repeat_interleave(w.k, 0))
+    assert torch.equal(xp[ros], inp["x"].cpu().repeat_interleave(w.k, 0))
     tor = layer.token_of_row.cpu()
     used = int(layer.tile_offsets[-1]) * 128
     pad = (tor[:used] < 0).nonzero().view(-1)
@@ -93,11 +93,14 @@ def test_permute_is_exact_copy_and_padding_is_zero():
 def test_repeat_runs_are_bitwise_identical():
     w = moe_inputs.small("det", T=2048, d=256, E=32, k=4, f=256, routing="zipf", alpha=0.8)
     l1, r1, inp = _run(w)
-    snap = {k: getattr(l1, k).clone() for k in ("row_of_slot", "token_of_row", "out")}
+    used = int(l1.tile_offsets[-1]) * 128          # rows past the groups are never written
+    snap = {k: getattr(l1, k).clone() for k in ("row_of_slot", "out", "counts", "tile_offsets")}
+    snap["token_of_row"] = l1.token_of_row[:used].clone()
     snap.update({k: v.clone() for k, v in r1.items()})
     l2, r2, _ = _run(w, inp)
-    for k in ("row_of_slot", "token_of_row", "out"):
+    for k in ("row_of_slot", "out", "counts", "tile_offsets"):
         assert torch.equal(getattr(l2, k), snap[k]), k
+    assert torch.equal(l2.token_of_row[:used], snap["token_of_row"])
     for k, v in r2.items():
         assert torch.equal(v, snap[k]), k
 
