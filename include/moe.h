@@ -102,6 +102,31 @@ int moe_count_index(const int32_t *topk_idx, int T, int k, int E, int32_t *count
                     size_t ws_bytes, moe_stream_t stream);
 
 /* ---------------------------------------------------------------------------------------------
+ * moe_count_index without a workspace. The paper has no counterpart: this entry point exists for
+ * callers that cannot allocate device memory (for example a plugin inside a host framework that
+ * owns all device allocations and passes only input and output buffers, or a service that forbids
+ * allocation after start-up). Arguments, outputs and results are those of moe_count_index; the
+ * scratch lives in a fixed device array of MOE_STATIC_SCRATCH_BYTES inside the library, present on
+ * every GPU that loads the library until the process exits.
+ *   - Size limit: calls whose moe_count_index_workspace_size(T, k, E) exceeds
+ *     MOE_STATIC_SCRATCH_BYTES return MOE_ERR_UNSUPPORTED (1 MiB covers, e.g., T*k = 1M slots at
+ *     E = 64, or T*k = 262,144 slots at E = 256).
+ *   - The first call on a device looks up the array's device address (cudaGetSymbolAddress) and
+ *     caches it; make that first call before any stream capture on that device.
+ *   - Every call on a device shares the one array: calls that overlap on the GPU (different streams
+ *     without ordering between them) race and give wrong results. Each call clears what must start
+ *     at zero, so consecutive calls are independent.
+ *   - Device-detected errors (a bad expert id, a look-back wait that ran out) are not reported to
+ *     the caller; slots with a bad id still get row_of_slot = -1. Use moe_count_index with a
+ *     workspace where the device status is needed.
+ *   - Allocates nothing: no cudaMalloc, cudaFree or allocating library call.
+ */
+#define MOE_STATIC_SCRATCH_BYTES (1 << 20)
+int moe_count_index_static(const int32_t *topk_idx, int T, int k, int E, int32_t *counts, int32_t *offsets,
+                           int32_t *tile_offsets, int32_t *row_of_slot, int32_t *token_of_row,
+                           moe_stream_t stream);
+
+/* ---------------------------------------------------------------------------------------------
  * Token permutation into the grouped layout (the consumer of the generated indices; brief,
  * section 核心方法). x [T, d] -> x_perm [rows_max, d]: x_perm[row_of_slot[t*k+j]] = x[t]; padding
  * rows of every expert are written with zeros. Each x row is read once and written k times.

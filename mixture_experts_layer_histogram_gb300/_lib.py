@@ -31,6 +31,7 @@ _SIGS = {
     "moe_count_index_workspace_size": (_SZ, [_I, _I, _I]),
     "moe_count_index_hook_offset": (_SZ, [_I]),
     "moe_count_index": (_I, [_P, _I, _I, _I, _P, _P, _P, _P, _P, _P, _SZ, _P]),
+    "moe_count_index_static": (_I, [_P, _I, _I, _I, _P, _P, _P, _P, _P, _P]),
     "moe_permute": (_I, [_P, _I, _I, _I, _I, _I, _P, _P, _P, _I64, _P, _P]),
     "moe_grouped_ffn_workspace_size": (_SZ, [_I, _I, _I, _I64, _I, _I]),
     "moe_grouped_ffn_fwd": (_I, [_P, _P, _P, _P, _I, _I, _I, _I64, _I, _P, _P, _P, _P, _SZ, _P]),
@@ -117,6 +118,14 @@ def moe_count_index(topk_idx, E, counts, offsets, tile_offsets, row_of_slot, tok
     _ok("moe_count_index", lib().moe_count_index(_p(topk_idx), T, k, E, _p(counts), _p(offsets), _p(tile_offsets),
                                                  _p(row_of_slot), _p(token_of_row), _p(ws), ws.numel() * ws.element_size(),
                                                  _s(stream)))
+
+
+def moe_count_index_static(topk_idx, E, counts, offsets, tile_offsets, row_of_slot, token_of_row, stream=None):
+    """moe_count_index for callers that cannot allocate: the scratch is a fixed array inside libmoe."""
+    T, k = topk_idx.shape
+    _ok("moe_count_index_static", lib().moe_count_index_static(
+        _p(topk_idx), T, k, E, _p(counts), _p(offsets), _p(tile_offsets), _p(row_of_slot), _p(token_of_row),
+        _s(stream)))
 
 
 def moe_permute(x, k, E, row_of_slot, counts, tile_offsets, x_perm, stream=None):

@@ -334,3 +334,71 @@ extern "C" size_t moe_count_index_hook_offset(int E) {
   if (E < 1) return 0;
   return sizeof(IndexWs) + acc_bytes(E);
 }
+
+// ---------------------------------------------------------------------------------------------
+// Allocation-free variant of moe_count_index.
+//
+// Some callers cannot allocate device memory at all: a plugin inside a host framework that owns
+// every device allocation and hands the plugin only its input and output buffers, or a service
+// that forbids allocation once it has started. They cannot provide the workspace that
+// moe_count_index needs, so this variant keeps that scratch in a fixed array in the library's own
+// device memory. The array exists on every GPU that loads the library, for the life of the
+// process, and is shared by all calls on that GPU.
+static __device__ __align__(256) unsigned char g_count_index_scratch[MOE_STATIC_SCRATCH_BYTES];
+
+#include <mutex>
+
+// The array's name is only a host-side stand-in, not a device address; each device's address is
+// looked up once (with that device current) and cached.
+static int static_scratch_address(void **out) {
+  static std::mutex mu;
+  static void *addr[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return MOE_ERR_CUDA;
+  }
+  if (dev < 0 || dev >= 64) return MOE_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lock(mu);
+  if (addr[dev] == nullptr) {
+    void *p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_count_index_scratch) != cudaSuccess || p == nullptr) {
+      (void)cudaGetLastError();
+      return MOE_ERR_CUDA;
+    }
+    addr[dev] = p;
+  }
+  *out = addr[dev];
+  return MOE_OK;
+}
+
+extern "C" int moe_count_index_static(const int32_t *topk_idx, int T, int k, int E, int32_t *counts,
+                                      int32_t *offsets, int32_t *tile_offsets, int32_t *row_of_slot,
+                                      int32_t *token_of_row, moe_stream_t stream) {
+  if (T < 0 || E < 1 || E > MOE_MAX_EXPERTS || k < 1 || k > MOE_MAX_TOPK) return MOE_ERR_INVALID_ARG;
+  if ((int64_t)T * k >= (int64_t)1 << 31) return MOE_ERR_UNSUPPORTED;
+  if (!counts || !offsets || !tile_offsets || !token_of_row) return MOE_ERR_INVALID_ARG;
+  if (T > 0 && (!topk_idx || !row_of_slot)) return MOE_ERR_INVALID_ARG;
+  if (moe_count_index_workspace_size(T, k, E) > (size_t)MOE_STATIC_SCRATCH_BYTES) return MOE_ERR_UNSUPPORTED;
+  void *scratch = nullptr;
+  int rc = static_scratch_address(&scratch);
+  if (rc != MOE_OK) return rc;
+  cudaStream_t s = (cudaStream_t)stream;
+  char *w = static_cast<char *>(scratch);
+  IndexWs *iw = reinterpret_cast<IndexWs *>(w);
+  int32_t *acc = reinterpret_cast<int32_t *>(w + sizeof(IndexWs));
+  int32_t *hook = reinterpret_cast<int32_t *>(w + sizeof(IndexWs) + acc_bytes(E));
+  uint64_t *lookback = reinterpret_cast<uint64_t *>(w + sizeof(IndexWs) + acc_bytes(E) + kHookBytes);
+  // The array keeps the previous call's contents: reset the status word, tickets, histogram
+  // accumulator and fault hook here; the count kernel resets the look-back words it uses.
+  MOE_TRY_CUDA(cudaMemsetAsync(w, 0, sizeof(IndexWs) + acc_bytes(E) + kHookBytes, s));
+  const int64_t n = (int64_t)T * k;
+  const int nb = (int)(n > 0 ? index_blocks(T, k) : 1);
+  count_kernel<<<nb, kIdxThreads, 0, s>>>(topk_idx, n, E, MOE_GROUP_ROWS, &iw->hdr, acc, hook, lookback, counts,
+                                          offsets, tile_offsets);
+  MOE_CHECK_LAUNCH();
+  index_kernel<<<nb, kIdxThreads, 0, s>>>(topk_idx, n, k, E, MOE_GROUP_ROWS, &iw->hdr, lookback, counts,
+                                          tile_offsets, row_of_slot, token_of_row);
+  MOE_CHECK_LAUNCH();
+  return MOE_OK;
+}
