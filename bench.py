@@ -49,7 +49,7 @@ def _dist():
 
 
 class ClockSampler:
-    """nvidia-smi clock / throttle-reason samples during the timed region."""
+    """nvidia-smi clock / throttle-reason samples, kept only if taken inside the timed window."""
 
     Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
          "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
@@ -58,33 +58,44 @@ class ClockSampler:
     def __init__(self, gpu_index):
         self.gpu = gpu_index
         self.proc = None
+        self.samples = []          # (host time, csv line)
+        self.window = None
 
-    def __enter__(self):
+    def start(self):
+        import threading
         try:
             self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.Q}",
-                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                          "--format=csv,noheader,nounits", "-lms", "50"],
                                          stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except Exception:
             self.proc = None
+            return self
+
+        def reader():
+            for ln in self.proc.stdout:
+                if ln.strip():
+                    self.samples.append((time.time(), ln))
+
+        self.thread = threading.Thread(target=reader, daemon=True)
+        self.thread.start()
         return self
 
-    def __exit__(self, *a):
-        self.lines = []
+    def stop(self):
         if self.proc is not None:
             self.proc.terminate()
             try:
-                out, _ = self.proc.communicate(timeout=5)
+                self.proc.wait(timeout=5)
             except Exception:
                 self.proc.kill()
-                out = ""
-            self.lines = [ln for ln in out.splitlines() if ln.strip()]
 
     def summary(self):
-        if not getattr(self, "lines", None):
+        if not self.samples or self.window is None:
             return None
+        t0, t1 = self.window
+        lines = [ln for ts, ln in self.samples if t0 <= ts <= t1 + 0.05]
         sm, mx, reasons = [], None, set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ln in self.lines:
+        for ln in lines:
             f = [x.strip() for x in ln.split(",")]
             try:
                 sm.append(float(f[1]))
@@ -150,6 +161,7 @@ def run_ours(args):
         L.moe_combine_fwd(layer.dx_perm, None, layer.row_of_slot, w.T, w.k, layer.dx)
         ev[8].record(stream)
 
+    clk = ClockSampler(dev.index).start()
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize(dev)
@@ -164,12 +176,14 @@ def run_ours(args):
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize(dev)
-    with ClockSampler(dev.index) as clk:
-        t_start.record(stream)
-        for i in range(args.steps):
-            step(evs[i])
-        t_end.record(stream)
-        torch.cuda.synchronize(dev)
+    w0 = time.time()
+    t_start.record(stream)
+    for i in range(args.steps):
+        step(evs[i])
+    t_end.record(stream)
+    torch.cuda.synchronize(dev)
+    clk.window = (w0, time.time())
+    clk.stop()
     if world > 1:
         dist.barrier()
     elapsed_ms = t_start.elapsed_time(t_end)
@@ -334,8 +348,8 @@ def run_reference(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
-    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=12.0)

@@ -6,8 +6,9 @@
 //
 //   warp 0      TMA producer: 128B-swizzled tiles of A and B into a 4-stage shared-memory ring
 //   warp 1      allocates the 512 TMEM columns, issues tcgen05.mma (one thread), commits to barriers
-//   warps 2..5  epilogue: tcgen05.ld of the fp32 accumulator (double-buffered in TMEM, 2 x 256
-//               columns) -> fused SwiGLU / SwiGLU-backward / plain -> bf16 -> global
+//   warps 2..9  epilogue: tcgen05.ld of the fp32 accumulator (double-buffered in TMEM, 2 x 256
+//               columns) -> fused SwiGLU / SwiGLU-backward / plain -> bf16 -> global; two warps
+//               share each 32-lane TMEM quarter and take one half of the tile's columns each
 //
 // Tile 128 x 256 x 64 (bf16 in, fp32 accumulate). Every expert's row group is padded to 128 rows,
 // so every tile belongs to one expert and is full; the tile scheduler walks the flattened tile
@@ -32,7 +33,9 @@ constexpr int BM = 128, BN = 256, BK = 64, STAGES = 4;
 constexpr int A_BYTES = BM * BK * 2;        // 16 KB
 constexpr int B_BYTES = BN * BK * 2;        // 32 KB
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-constexpr int THREADS = 192;
+constexpr int EPI_WARPS = 8;                // two warps per TMEM lane quarter, each drains half the columns
+constexpr int EPI_THREADS = EPI_WARPS * 32;
+constexpr int THREADS = 64 + EPI_THREADS;
 constexpr int TMEM_COLS = 2 * BN;           // two fp32 accumulators of 128 lanes x 256 columns
 constexpr int MAX_E = MOE_MAX_EXPERTS;
 constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + 256 + (MAX_E + 1) * 4;
@@ -189,8 +192,10 @@ __device__ __forceinline__ void store_row_bf16(__nv_bfloat16 *dst, const float *
   for (int i = 0; i < 4; ++i) q[i] = pack_bf16x8(v + 8 * i);
 }
 
+// Columns [c0, c0 + cols) of the accumulator (GATEUP: of each half) for one row of the tile.
 template <int KIND>
-__device__ __forceinline__ void epilogue_tile(const Tile &t, const Params &p, uint32_t tbase, int row_in_tile) {
+__device__ __forceinline__ void epilogue_tile(const Tile &t, const Params &p, uint32_t tbase, int row_in_tile,
+                                              int c0, const uint4 (&pre)[8]) {
   float v[32];
   uint32_t r[32];
   if (KIND == GATEUP) {
@@ -198,7 +203,7 @@ __device__ __forceinline__ void epilogue_tile(const Tile &t, const Params &p, ui
     __nv_bfloat16 *ab = p.out0 + grow * p.ld0;
     __nv_bfloat16 *h = p.out1 + grow * p.ld1;
 #pragma unroll 1
-    for (int c = 0; c < BN / 2; c += 32) {
+    for (int c = c0; c < c0 + BN / 4; c += 32) {
       uint32_t rb[32];
       tmem_ld32(tbase + c, r);
       tmem_ld32(tbase + BN / 2 + c, rb);
@@ -216,19 +221,32 @@ __device__ __forceinline__ void epilogue_tile(const Tile &t, const Params &p, ui
       store_row_bf16(h + t.n0 + c, hv);
     }
   } else if (KIND == DH) {
+    // a and b of the current 32 columns arrive one chunk ahead (the first chunk was loaded
+    // before the accumulator was ready): the loads' latency overlaps the previous chunk's work.
     const int64_t grow = t.m0 + row_in_tile;
     const __nv_bfloat16 *abrow = p.aux + grow * p.ld_aux;
     __nv_bfloat16 *dab = p.out0 + grow * p.ld0;
+    uint4 cur[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) cur[i] = pre[i];
 #pragma unroll 1
-    for (int c = 0; c < BN; c += 32) {
+    for (int c = c0; c < c0 + BN / 2; c += 32) {
+      uint4 nxt[8];
+      if (c + 32 < c0 + BN / 2) {
+        const uint4 *qa = reinterpret_cast<const uint4 *>(abrow + t.n0 + c + 32);
+        const uint4 *qb = reinterpret_cast<const uint4 *>(abrow + p.f + t.n0 + c + 32);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          nxt[i] = qa[i];
+          nxt[4 + i] = qb[i];
+        }
+      }
       tmem_ld32(tbase + c, r);
-      const uint4 *qa = reinterpret_cast<const uint4 *>(abrow + t.n0 + c);
-      const uint4 *qb = reinterpret_cast<const uint4 *>(abrow + p.f + t.n0 + c);
       float av[32], bv[32], db[32];
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
-        unpack_bf16x8(qa[i], av + 8 * i);
-        unpack_bf16x8(qb[i], bv + 8 * i);
+        unpack_bf16x8(cur[i], av + 8 * i);
+        unpack_bf16x8(cur[4 + i], bv + 8 * i);
       }
       tmem_ld_wait();
 #pragma unroll
@@ -239,13 +257,15 @@ __device__ __forceinline__ void epilogue_tile(const Tile &t, const Params &p, ui
       }
       store_row_bf16(dab + t.n0 + c, v);
       store_row_bf16(dab + p.f + t.n0 + c, db);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) cur[i] = nxt[i];
     }
   } else {
     __nv_bfloat16 *dst;
     if (KIND == WGRAD) dst = p.out0 + (int64_t)t.e * p.out_e_stride + (int64_t)(t.m0 + row_in_tile) * p.ld0 + t.n0;
     else dst = p.out0 + (int64_t)(t.m0 + row_in_tile) * p.ld0 + t.n0;
 #pragma unroll 1
-    for (int c = 0; c < BN; c += 32) {
+    for (int c = c0; c < c0 + BN / 2; c += 32) {
       tmem_ld32(tbase + c, r);
       tmem_ld_wait();
 #pragma unroll
@@ -285,7 +305,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(tfull_bar(a), 1);
-      mbar_init(tempty_bar(a), 128);
+      mbar_init(tempty_bar(a), EPI_THREADS);
     }
     mbar_init(mma_done_bar, 1);
     *abort_flag = 0;
@@ -391,22 +411,34 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
   } else if (warp >= 2) {
     // ------------------------------------------------------------------ epilogue
-    const int quarter = warp & 3;   // TMEM lanes this warp may access: 32 * quarter ...
+    const int quarter = warp & 3;                       // TMEM lanes this warp may access: 32 * quarter ...
+    const int half = (warp - 2) >> 2;                   // which half of the tile's columns
     const int row_in_tile = quarter * 32 + lane;
+    const int c0 = half * (KIND == GATEUP ? BN / 4 : BN / 2);
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
       const Tile t = decode<KIND>(tile, p, toff);
       if (t.kb == 0) {   // WGRAD of an expert with no rows: the gradient is zero
-        __nv_bfloat16 *dst = p.out0 + (int64_t)t.e * p.out_e_stride + (int64_t)(t.m0 + row_in_tile) * p.ld0 + t.n0;
+        __nv_bfloat16 *dst =
+            p.out0 + (int64_t)t.e * p.out_e_stride + (int64_t)(t.m0 + row_in_tile) * p.ld0 + t.n0 + c0;
         uint4 *q = reinterpret_cast<uint4 *>(dst);
-        for (int i = 0; i < BN / 8; ++i) q[i] = make_uint4(0, 0, 0, 0);
+        for (int i = 0; i < BN / 16; ++i) q[i] = make_uint4(0, 0, 0, 0);
         continue;
+      }
+      uint4 pre[8];
+      if (KIND == DH) {   // first chunk of a, b: independent of the MMA, load before waiting
+        const __nv_bfloat16 *abrow = p.aux + (int64_t)(t.m0 + row_in_tile) * p.ld_aux + t.n0 + c0;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          pre[i] = reinterpret_cast<const uint4 *>(abrow)[i];
+          pre[4 + i] = reinterpret_cast<const uint4 *>(abrow + p.f)[i];
+        }
       }
       if (!mbar_wait(tfull_bar(acc), acc_phase, abort_flag, p.hdr, 4)) break;
       tc_fence_after();
       const uint32_t tbase = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * BN);
-      epilogue_tile<KIND>(t, p, tbase, row_in_tile);
+      epilogue_tile<KIND>(t, p, tbase, row_in_tile, c0, pre);
       tc_fence_before();
       mbar_arrive(tempty_bar(acc));
       acc ^= 1;
