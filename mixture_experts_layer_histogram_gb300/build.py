@@ -42,7 +42,7 @@ def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
     os.makedirs(BUILD, exist_ok=True)
     dep_t = _deps()
     flags = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", f"-I{INCLUDE}", f"-I{CSRC}",
-                    "--expt-relaxed-constexpr"] + list(extra_flags)
+                    "--expt-relaxed-constexpr"] + list(extra_flags) + os.environ.get("MOE_NVCC_FLAGS", "").split()
     jobs = []
     objs = []
     for src in SOURCES:

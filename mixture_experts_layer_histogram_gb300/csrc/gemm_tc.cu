@@ -25,6 +25,7 @@
 #include <cuda.h>
 
 #include "common.cuh"
+#include "tc_ptx.cuh"
 
 namespace moe {
 namespace tc {
@@ -38,7 +39,7 @@ constexpr int EPI_THREADS = EPI_WARPS * 32;
 constexpr int THREADS = 64 + EPI_THREADS;
 constexpr int TMEM_COLS = 2 * BN;           // two fp32 accumulators of 128 lanes x 256 columns
 constexpr int MAX_E = MOE_MAX_EXPERTS;
-constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + 256 + (MAX_E + 1) * 4;
+constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 32 * 32 * 2 * 2 * EPI_WARPS + 1024 + 256;
 
 enum Kind { GATEUP = 0, DOWN = 1, DH = 2, DGRAD = 3, WGRAD = 4 };
 
@@ -58,88 +59,6 @@ struct Params {
   int64_t ld_aux;
   int64_t out_e_stride;
 };
-
-// ----------------------------------------------------------------------------- PTX wrappers ----
-__device__ __forceinline__ uint32_t smem_u32(const void *p) { return (uint32_t)__cvta_generic_to_shared(p); }
-
-__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
-}
-__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
-}
-__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
-}
-__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-
-// Bounded wait for the phase with parity `parity` of barrier `bar`. False = gave up (timeout or abort).
-__device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int *abort_flag, WsHeader *hdr,
-                                       int where) {
-  if (mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = global_ns();
-  while (true) {
-#pragma unroll 1
-    for (int i = 0; i < 32; ++i)
-      if (mbar_try_wait(bar, parity)) return true;
-    if (*abort_flag) return false;
-    if (global_ns() - t0 > kWaitLimitNs) {
-      report(hdr, MOE_ERR_DEVICE_TIMEOUT, where);
-      *abort_flag = 1;
-      return false;
-    }
-  }
-}
-
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, int x, int y, uint32_t bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
-      : "memory");
-}
-
-__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
-__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
-
-__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
-                                         uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate));
-}
-__device__ __forceinline__ void mma_commit(uint32_t bar) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
-}
-
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
-      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
-        "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]),
-        "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
-        "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
-      : "r"(taddr));
-}
-__device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
-
-// Shared-memory matrix descriptor (tcgen05), 128-byte swizzle, SM100 descriptor version 1.
-__device__ __forceinline__ uint64_t sdesc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
-  return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
-         ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (2ull << 61);
-}
 
 // Instruction descriptor, kind::f16: D fp32, A and B bf16, M = 128, N = 256, K-major unless *_mn.
 __host__ __device__ constexpr uint32_t idesc_bf16(bool a_mn, bool b_mn) {
@@ -186,22 +105,56 @@ __device__ __forceinline__ Tile decode(int tile, const Params &p, const int *tof
 }
 
 // ----------------------------------------------------------------------------- epilogues -------
-__device__ __forceinline__ void store_row_bf16(__nv_bfloat16 *dst, const float *v) {   // 32 values, 64 B
-  uint4 *q = reinterpret_cast<uint4 *>(dst);
-#pragma unroll
-  for (int i = 0; i < 4; ++i) q[i] = pack_bf16x8(v + 8 * i);
-}
+// Output path: each epilogue warp converts 32 rows x 32 columns to bf16, writes them into one of
+// its two 2 KB shared-memory buffers (64-byte swizzle: 16-byte chunk c of row r goes to chunk
+// c ^ ((r >> 1) & 3), which keeps the 32 lanes' writes free of bank conflicts), and one lane
+// stores the block with a TMA bulk tensor store. The L2 then sees whole-line writes instead of
+// one 16-byte partial-sector request per thread and row.
+constexpr int EPI_BUF_BYTES = 32 * 32 * 2;                 // one 32 x 32 bf16 block
+constexpr int EPI_STAGE_BYTES = EPI_WARPS * 2 * EPI_BUF_BYTES;
 
-// Columns [c0, c0 + cols) of the accumulator (GATEUP: of each half) for one row of the tile.
+struct EpiStore {
+  uint32_t buf;   // this warp's two buffers (shared::cta address, 1024-aligned region)
+  int bi;
+  int lane;
+  __device__ __forceinline__ void put(const CUtensorMap *map, int x, int y, const float *v) {
+    const uint32_t b = buf + (uint32_t)bi * EPI_BUF_BYTES;
+    if (lane == 0) asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");   // b's previous store has read it
+    __syncwarp();
+    const uint32_t row = b + (uint32_t)lane * 64, sw = (uint32_t)(lane >> 1) & 3u;
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      const uint4 q = pack_bf16x8(v + 8 * c);
+      asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(row + ((c ^ sw) << 4)), "r"(q.x), "r"(q.y), "r"(q.z),
+                   "r"(q.w)
+                   : "memory");
+    }
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // visible to the TMA (async proxy)
+    __syncwarp();
+    if (lane == 0) {
+      asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
+                       reinterpret_cast<uint64_t>(map)),
+                   "r"(x), "r"(y), "r"(b)
+                   : "memory");
+      asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+    }
+    bi ^= 1;
+  }
+  __device__ __forceinline__ void drain() {
+    if (lane == 0) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+    __syncwarp();
+  }
+};
+
+// Columns [c0, c0 + cols) of the accumulator (GATEUP: of each half) for the warp's 32 rows; `row`
+// is this thread's row in the tile, `yrow` the global row (in the output map) of the warp's first row.
 template <int KIND>
-__device__ __forceinline__ void epilogue_tile(const Tile &t, const Params &p, uint32_t tbase, int row_in_tile,
-                                              int c0, const uint4 (&pre)[8]) {
+__device__ __forceinline__ void epilogue_tile(const Tile &t, const Params &p, uint32_t tbase, int row, int yrow, int c0,
+                                              const uint4 (&pre)[8], EpiStore &es, const CUtensorMap *mc0,
+                                              const CUtensorMap *mc1) {
   float v[32];
   uint32_t r[32];
   if (KIND == GATEUP) {
-    const int64_t grow = t.m0 + row_in_tile;
-    __nv_bfloat16 *ab = p.out0 + grow * p.ld0;
-    __nv_bfloat16 *h = p.out1 + grow * p.ld1;
 #pragma unroll 1
     for (int c = c0; c < c0 + BN / 4; c += 32) {
       uint32_t rb[32];
@@ -216,16 +169,14 @@ __device__ __forceinline__ void epilogue_tile(const Tile &t, const Params &p, ui
         bv[i] = b;
         hv[i] = a * sigmoidf_(a) * b;
       }
-      store_row_bf16(ab + t.n0 + c, v);
-      store_row_bf16(ab + p.f + t.n0 + c, bv);
-      store_row_bf16(h + t.n0 + c, hv);
+      es.put(mc0, t.n0 + c, yrow, v);           // a  -> ab[:, n0 + c]
+      es.put(mc0, p.f + t.n0 + c, yrow, bv);    // b  -> ab[:, f + n0 + c]
+      es.put(mc1, t.n0 + c, yrow, hv);          // h
     }
   } else if (KIND == DH) {
     // a and b of the current 32 columns arrive one chunk ahead (the first chunk was loaded
     // before the accumulator was ready): the loads' latency overlaps the previous chunk's work.
-    const int64_t grow = t.m0 + row_in_tile;
-    const __nv_bfloat16 *abrow = p.aux + grow * p.ld_aux;
-    __nv_bfloat16 *dab = p.out0 + grow * p.ld0;
+    const __nv_bfloat16 *abrow = p.aux + (int64_t)(t.m0 + row) * p.ld_aux;
     uint4 cur[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) cur[i] = pre[i];
@@ -255,39 +206,44 @@ __device__ __forceinline__ void epilogue_tile(const Tile &t, const Params &p, ui
         v[i] = dh * bv[i] * s * (1.0f + a * (1.0f - s));
         db[i] = dh * a * s;
       }
-      store_row_bf16(dab + t.n0 + c, v);
-      store_row_bf16(dab + p.f + t.n0 + c, db);
+      es.put(mc0, t.n0 + c, yrow, v);           // da -> dab[:, n0 + c]
+      es.put(mc0, p.f + t.n0 + c, yrow, db);    // db -> dab[:, f + n0 + c]
 #pragma unroll
       for (int i = 0; i < 8; ++i) cur[i] = nxt[i];
     }
   } else {
-    __nv_bfloat16 *dst;
-    if (KIND == WGRAD) dst = p.out0 + (int64_t)t.e * p.out_e_stride + (int64_t)(t.m0 + row_in_tile) * p.ld0 + t.n0;
-    else dst = p.out0 + (int64_t)(t.m0 + row_in_tile) * p.ld0 + t.n0;
 #pragma unroll 1
     for (int c = c0; c < c0 + BN / 2; c += 32) {
       tmem_ld32(tbase + c, r);
       tmem_ld_wait();
 #pragma unroll
       for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
-      store_row_bf16(dst + c, v);
+      es.put(mc0, t.n0 + c, yrow, v);
     }
   }
+}
+
+// Global row (in the output tensor map) of the first of the 32 rows a warp stores.
+template <int KIND>
+__device__ __forceinline__ int epi_yrow(const Tile &t, const Params &p, int quarter) {
+  return KIND == WGRAD ? t.e * (p.m_tiles * BM) + t.m0 + quarter * 32 : t.m0 + quarter * 32;
 }
 
 // ----------------------------------------------------------------------------- the kernel ------
 template <int KIND>
 __global__ void __launch_bounds__(THREADS, 1)
-    tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, const Params p) {
+    tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                   const __grid_constant__ CUtensorMap tmC0, const __grid_constant__ CUtensorMap tmC1, const Params p) {
   constexpr bool A_MN = (KIND == WGRAD);
   constexpr bool B_MN = (KIND == DH || KIND == DGRAD || KIND == WGRAD);
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint64_t *bars = reinterpret_cast<uint64_t *>(smem + STAGES * STAGE_BYTES);
+  uint8_t *epi_smem = smem + STAGES * STAGE_BYTES;
+  uint64_t *bars = reinterpret_cast<uint64_t *>(epi_smem + EPI_STAGE_BYTES);
   // bars: full[STAGES], empty[STAGES], tfull[2], tempty[2], mma_done
   uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(bars + 2 * STAGES + 5);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_holder + 1);
-  int *toff = reinterpret_cast<int *>(tmem_holder + 4);
+  const int *toff = p.tile_offsets;   // read through L1; shared memory goes to the ring
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t sbase = smem_u32(smem);
@@ -313,7 +269,6 @@ __global__ void __launch_bounds__(THREADS, 1)
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmA)) : "memory");
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmB)) : "memory");
   }
-  for (int i = threadIdx.x; i <= p.E; i += THREADS) toff[i] = p.tile_offsets[i];
   if (warp == 1) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_holder)),
                  "r"((uint32_t)TMEM_COLS)
@@ -415,6 +370,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     const int half = (warp - 2) >> 2;                   // which half of the tile's columns
     const int row_in_tile = quarter * 32 + lane;
     const int c0 = half * (KIND == GATEUP ? BN / 4 : BN / 2);
+    EpiStore es{smem_u32(epi_smem) + (uint32_t)(warp - 2) * 2 * EPI_BUF_BYTES, 0, lane};
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
@@ -438,12 +394,13 @@ __global__ void __launch_bounds__(THREADS, 1)
       if (!mbar_wait(tfull_bar(acc), acc_phase, abort_flag, p.hdr, 4)) break;
       tc_fence_after();
       const uint32_t tbase = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * BN);
-      epilogue_tile<KIND>(t, p, tbase, row_in_tile, c0, pre);
+      epilogue_tile<KIND>(t, p, tbase, row_in_tile, epi_yrow<KIND>(t, p, quarter), c0, pre, es, &tmC0, &tmC1);
       tc_fence_before();
       mbar_arrive(tempty_bar(acc));
       acc ^= 1;
       if (acc == 0) acc_phase ^= 1u;
     }
+    es.drain();
   }
 
   tc_fence_before();
@@ -451,6 +408,292 @@ __global__ void __launch_bounds__(THREADS, 1)
   if (warp == 1) {
     tc_fence_after();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"((uint32_t)TMEM_COLS)
+                 : "memory");
+  }
+}
+
+// ----------------------------------------------------------------------------- CTA-pair kernel --
+// A cluster of two CTAs (one TPC) computes a 256 x 256 tile with tcgen05.mma.cta_group::2: CTA r
+// holds rows [128 r, 128 r + 128) of A and half r of B (N rows [128 r, 128 r + 128)) in its own
+// shared memory, and receives its 128 rows x 256 columns of the accumulator in its own TMEM. Each
+// SM therefore loads 32 KB per 64-deep k-block instead of 48 KB for the same MMA work. The leader
+// (rank 0) issues the MMAs; both CTAs' TMA loads complete on the leader's full barrier; the MMA
+// commits multicast to both CTAs' empty / accumulator-full barriers; both epilogues arrive on the
+// leader's accumulator-empty barrier. Row-grouped kinds pair two consecutive row tiles of one
+// expert; when an expert has an odd number of row tiles, the second CTA of its last pair computes
+// rows past the expert and discards them.
+constexpr int P_BK = 64;                        // k depth of one ring stage (a multiple of 64)
+constexpr int P_KA = P_BK / 64;                 // 128-byte swizzle atoms along k per stage
+constexpr int P_STAGES = 6;
+constexpr int P_A_BYTES = BM * P_BK * 2;        // this CTA's 128 rows of A
+constexpr int P_B_BYTES = (BN / 2) * P_BK * 2;  // this CTA's half of B
+constexpr int P_STAGE_BYTES = P_A_BYTES + P_B_BYTES;
+constexpr int P_SMEM_BYTES = P_STAGES * P_STAGE_BYTES + EPI_STAGE_BYTES + 1024 + 160 + (MAX_E + 1) * 4;
+static_assert(P_SMEM_BYTES <= 232448, "pair kernel shared memory exceeds 227 KB");
+
+// Instruction descriptor for the pair MMA: M = 256 (128 rows per CTA), N = 256.
+__host__ __device__ constexpr uint32_t idesc_bf16_pair(bool a_mn, bool b_mn) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((a_mn ? 1u : 0u) << 15) | ((b_mn ? 1u : 0u) << 16) |
+         ((uint32_t)(BN >> 3) << 17) | ((uint32_t)((2 * BM) >> 4) << 24);
+}
+
+// The pair tile as seen from CTA `rank`; valid = false when this CTA's row tile lies past its expert.
+template <int KIND>
+__device__ __forceinline__ Tile decode_pair(int tile, const Params &p, const int *toff, const int *ptoff, int rank,
+                                            bool &valid) {
+  Tile t;
+  valid = true;
+  if (KIND == WGRAD) {
+    const int per = (p.m_tiles / 2) * p.n_tiles;
+    t.e = tile / per;
+    const int r = tile - t.e * per;
+    t.m0 = (r / p.n_tiles) * (2 * BM) + rank * BM;
+    t.n0 = (r % p.n_tiles) * BN;
+    t.krow0 = toff[t.e] * BM;
+    t.kb = (toff[t.e + 1] - toff[t.e]) * (BM / P_BK);
+  } else {
+    const int pr = tile / p.n_tiles;
+    const int nt = tile - pr * p.n_tiles;
+    int lo = 0, hi = p.E - 1;   // last expert whose first pair row is <= pr
+    while (lo < hi) {
+      int mid = (lo + hi + 1) >> 1;
+      if (ptoff[mid] <= pr) lo = mid;
+      else hi = mid - 1;
+    }
+    t.e = lo;
+    const int rt = toff[t.e] + 2 * (pr - ptoff[t.e]) + rank;
+    valid = rt < toff[t.e + 1];
+    t.m0 = rt * BM;
+    t.n0 = nt * (KIND == GATEUP ? BN / 2 : BN);
+    t.kb = p.num_kb / P_KA;
+    t.krow0 = 0;
+  }
+  return t;
+}
+
+template <int KIND>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
+    tc_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                   const __grid_constant__ CUtensorMap tmC0, const __grid_constant__ CUtensorMap tmC1, const Params p) {
+  constexpr bool A_MN = (KIND == WGRAD);
+  constexpr bool B_MN = (KIND == DH || KIND == DGRAD || KIND == WGRAD);
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t *epi_smem = smem + P_STAGES * P_STAGE_BYTES;
+  uint64_t *bars = reinterpret_cast<uint64_t *>(epi_smem + EPI_STAGE_BYTES);
+  // bars: full[P_STAGES], empty[P_STAGES], tfull[2], tempty[2], mma_done
+  uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(bars + 2 * P_STAGES + 5);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_holder + 1);
+  int *ptoff = reinterpret_cast<int *>(tmem_holder + 4);
+  const int *toff = p.tile_offsets;   // read through L1; shared memory goes to the ring
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();
+  const bool leader = (rank == 0);
+  const uint32_t sbase = smem_u32(smem);
+  const uint32_t bar0 = smem_u32(bars);
+  auto full_bar = [&](int s) { return bar0 + 8u * s; };
+  auto empty_bar = [&](int s) { return bar0 + 8u * (P_STAGES + s); };
+  auto tfull_bar = [&](int a) { return bar0 + 8u * (2 * P_STAGES + a); };
+  auto tempty_bar = [&](int a) { return bar0 + 8u * (2 * P_STAGES + 2 + a); };
+  const uint32_t mma_done_bar = bar0 + 8u * (2 * P_STAGES + 4);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < P_STAGES; ++s) {
+      mbar_init(full_bar(s), 1);
+      mbar_init(empty_bar(s), 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(tfull_bar(a), 1);
+      mbar_init(tempty_bar(a), 2 * EPI_WARPS);   // one arrival per epilogue warp of both CTAs
+    }
+    mbar_init(mma_done_bar, 1);
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmA)) : "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmB)) : "memory");
+  }
+  __syncthreads();
+  if (KIND != WGRAD && warp == 0) {   // ptoff = exclusive scan of ceil(row tiles / 2) per expert
+    int c[8], sum = 0;
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      const int e = lane * 8 + q;
+      c[q] = e < p.E ? (toff[e + 1] - toff[e] + 1) / 2 : 0;
+      sum += c[q];
+    }
+    int incl = sum;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, incl, off);
+      if (lane >= off) incl += v;
+    }
+    int run = incl - sum;
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      const int e = lane * 8 + q;
+      if (e < p.E) ptoff[e] = run;
+      run += c[q];
+    }
+    if (lane == 31) ptoff[p.E] = incl;
+  }
+  if (warp == 1) {   // collective TMEM allocation by one warp of each CTA of the pair
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_holder)),
+                 "r"((uint32_t)TMEM_COLS)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  cluster_sync();   // both CTAs: barriers initialised, TMEM allocated
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_holder;
+
+  const int num_tiles = (KIND == WGRAD) ? p.E * (p.m_tiles / 2) * p.n_tiles : ptoff[p.E] * p.n_tiles;
+  const int cluster_id = blockIdx.x >> 1, num_clusters = gridDim.x >> 1;
+
+  if (warp == 0 && lane == 0) {
+    // ------------------------------------------------------------------ TMA producer (both CTAs)
+    // Boxes of k-block kb of tile t for this CTA, loaded into ring stage (sA, sB).
+    auto boxes = [&](const Tile &t, int kb, uint32_t sA, uint32_t sB, uint32_t fb) {
+      auto box = [&](const CUtensorMap *m, int x, int y, uint32_t dst) { tma_load_2d_pair(dst, m, x, y, fb); };
+      const int kx = kb * P_BK;
+      const int bn = t.n0 + (int)rank * (BN / 2);             // this CTA's half of B
+      if (KIND == GATEUP || KIND == DOWN) {                   // K-major A and B: one 64-wide box per atom
+        const int brow = t.e * p.b_rows_e + (KIND == GATEUP ? (rank ? p.f : 0) + t.n0 : bn);
+#pragma unroll
+        for (int a = 0; a < P_KA; ++a) {
+          box(&tmA, kx + 64 * a, t.m0, sA + a * (BM * 128));
+          box(&tmB, kx + 64 * a, brow, sB + a * ((BN / 2) * 128));
+        }
+      } else if (KIND == DH || KIND == DGRAD) {               // K-major A, MN-major B (64 x P_BK boxes)
+#pragma unroll
+        for (int a = 0; a < P_KA; ++a) box(&tmA, kx + 64 * a, t.m0, sA + a * (BM * 128));
+#pragma unroll
+        for (int q = 0; q < 2; ++q) box(&tmB, bn + 64 * q, t.e * p.b_rows_e + kx, sB + q * (P_BK * 128));
+      } else {   // WGRAD: MN-major A and B
+#pragma unroll
+        for (int q = 0; q < 2; ++q) box(&tmA, t.m0 + 64 * q, t.krow0 + kx, sA + q * (P_BK * 128));
+#pragma unroll
+        for (int q = 0; q < 2; ++q) box(&tmB, bn + 64 * q, t.krow0 + kx, sB + q * (P_BK * 128));
+      }
+    };
+    int stage = 0;
+    uint32_t phase = 0;
+    for (int tile = cluster_id; tile < num_tiles; tile += num_clusters) {
+      bool valid;
+      const Tile t = decode_pair<KIND>(tile, p, toff, ptoff, (int)rank, valid);
+      bool ok = true;
+      for (int kb = 0; kb < t.kb; ++kb) {
+        if (!mbar_wait_cluster(empty_bar(stage), phase ^ 1u, abort_flag, p.hdr, 11)) { ok = false; break; }
+        const uint32_t sA = sbase + stage * P_STAGE_BYTES, sB = sA + P_A_BYTES;
+        const uint32_t fb = mapa_shared(full_bar(stage), 0);   // the leader's full barrier
+        if (leader) mbar_expect_tx(full_bar(stage), 2 * P_STAGE_BYTES);
+        boxes(t, kb, sA, sB, fb);
+        if (++stage == P_STAGES) { stage = 0; phase ^= 1u; }
+      }
+      if (!ok) break;
+    }
+  } else if (warp == 1 && lane == 0 && leader) {
+    // ------------------------------------------------------------------ MMA issuer (leader only)
+    constexpr uint32_t idesc = idesc_bf16_pair(A_MN, B_MN);
+    int stage = 0, acc = 0;
+    uint32_t phase = 0, acc_phase = 0;
+    bool issued_any = false;
+    for (int tile = cluster_id; tile < num_tiles; tile += num_clusters) {
+      bool valid;
+      const Tile t = decode_pair<KIND>(tile, p, toff, ptoff, 0, valid);
+      if (t.kb == 0) continue;
+      if (!mbar_wait_cluster(tempty_bar(acc), acc_phase ^ 1u, abort_flag, p.hdr, 12)) break;
+      tc_fence_after();
+      const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
+      bool ok = true;
+      for (int kb = 0; kb < t.kb; ++kb) {
+        if (!mbar_wait_cluster(full_bar(stage), phase, abort_flag, p.hdr, 13)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t sA = sbase + stage * P_STAGE_BYTES, sB = sA + P_A_BYTES;
+#pragma unroll
+        for (int kk = 0; kk < P_BK / 16; ++kk) {
+          // K-major: atom kk/4 (128 rows x 128 B each), 32 B per 16-deep step inside the atom.
+          // MN-major: 2048 B per 16 k-rows; MN blocks of 64 are P_BK * 128 B apart.
+          const uint32_t koff = (uint32_t)((kk >> 2) * (BM * 128) + (kk & 3) * 32);
+          const uint64_t ad = A_MN ? sdesc(sA + kk * 2048, P_BK * 128, 1024) : sdesc(sA + koff, 16, 1024);
+          const uint64_t bd = B_MN ? sdesc(sB + kk * 2048, P_BK * 128, 1024) : sdesc(sB + koff, 16, 1024);
+          mma_bf16_pair(d_tmem, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
+        }
+        issued_any = true;
+        mma_commit_pair(empty_bar(stage), 0x3);   // frees this stage in both CTAs
+        if (++stage == P_STAGES) { stage = 0; phase ^= 1u; }
+      }
+      if (!ok) break;
+      mma_commit_pair(tfull_bar(acc), 0x3);       // both CTAs' accumulators are ready
+      acc ^= 1;
+      if (acc == 0) acc_phase ^= 1u;
+    }
+    if (issued_any) {
+      mma_commit_pair(mma_done_bar, 0x1);
+      const uint64_t t0 = global_ns();
+      while (!mbar_try_wait(mma_done_bar, 0) && global_ns() - t0 < kWaitLimitNs) {}
+    }
+  } else if (warp >= 2) {
+    // ------------------------------------------------------------------ epilogue (both CTAs)
+    const int quarter = warp & 3;
+    const int half = (warp - 2) >> 2;
+    const int row_in_tile = quarter * 32 + lane;
+    const int c0 = half * (KIND == GATEUP ? BN / 4 : BN / 2);
+    EpiStore es{smem_u32(epi_smem) + (uint32_t)(warp - 2) * 2 * EPI_BUF_BYTES, 0, lane};
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    for (int tile = cluster_id; tile < num_tiles; tile += num_clusters) {
+      bool valid;
+      const Tile t = decode_pair<KIND>(tile, p, toff, ptoff, (int)rank, valid);
+      if (t.kb == 0) {   // WGRAD of an expert with no rows: the gradient is zero
+        __nv_bfloat16 *dst =
+            p.out0 + (int64_t)t.e * p.out_e_stride + (int64_t)(t.m0 + row_in_tile) * p.ld0 + t.n0 + c0;
+        uint4 *q = reinterpret_cast<uint4 *>(dst);
+        for (int i = 0; i < BN / 16; ++i) q[i] = make_uint4(0, 0, 0, 0);
+        continue;
+      }
+      uint4 pre[8];
+      if (KIND == DH) {   // the next tile's a, b rows of this thread: into L2 now, read one tile later
+        const int nxt = tile + num_clusters;
+        if (nxt < num_tiles) {
+          bool nvalid;
+          const Tile tn = decode_pair<KIND>(nxt, p, toff, ptoff, (int)rank, nvalid);
+          if (nvalid) {
+            const __nv_bfloat16 *nrow = p.aux + (int64_t)(tn.m0 + row_in_tile) * p.ld_aux + tn.n0 + c0;
+            l2_prefetch_bytes(nrow, (BN / 2) * 2);
+            l2_prefetch_bytes(nrow + p.f, (BN / 2) * 2);
+          }
+        }
+      }
+      if (KIND == DH && valid) {
+        const __nv_bfloat16 *abrow = p.aux + (int64_t)(t.m0 + row_in_tile) * p.ld_aux + t.n0 + c0;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          pre[i] = reinterpret_cast<const uint4 *>(abrow)[i];
+          pre[4 + i] = reinterpret_cast<const uint4 *>(abrow + p.f)[i];
+        }
+      }
+      if (!mbar_wait_cluster(tfull_bar(acc), acc_phase, abort_flag, p.hdr, 14)) break;
+      tc_fence_after();
+      const uint32_t tbase = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * BN);
+      if (valid)
+        epilogue_tile<KIND>(t, p, tbase, row_in_tile, epi_yrow<KIND>(t, p, quarter), c0, pre, es, &tmC0, &tmC1);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster(mapa_shared(tempty_bar(acc), 0));
+      acc ^= 1;
+      if (acc == 0) acc_phase ^= 1u;
+    }
+    es.drain();
+  }
+
+  tc_fence_before();
+  cluster_sync();   // no CTA leaves while its peer may still signal its barriers or use its TMEM
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"((uint32_t)TMEM_COLS)
                  : "memory");
   }
 }
@@ -473,26 +716,56 @@ static EncodeTiledFn encode_fn() {
   return fn;
 }
 
-// 2D bf16 row-major [rows, cols], box = 64 columns (128 B, the swizzle span) x box_rows rows.
-static bool make_map(CUtensorMap *m, const void *base, uint64_t rows, uint64_t cols, uint32_t box_rows) {
+// 2D bf16 row-major [rows, cols] with box = box_cols x box_rows and the given swizzle.
+static bool encode_map(CUtensorMap *m, const void *base, uint64_t rows, uint64_t cols, uint32_t box_cols,
+                       uint32_t box_rows, CUtensorMapSwizzle swz) {
   EncodeTiledFn enc = encode_fn();
   if (!enc) return false;
   cuuint64_t dims[2] = {cols, rows};
   cuuint64_t strides[1] = {cols * 2};
-  cuuint32_t box[2] = {64, box_rows};
+  cuuint32_t box[2] = {box_cols, box_rows};
   cuuint32_t estr[2] = {1, 1};
   return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box, estr,
-             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
+// operand loads: 64 columns (128 B, the swizzle span) x box_rows rows, 128-byte swizzle
+static bool make_map(CUtensorMap *m, const void *base, uint64_t rows, uint64_t cols, uint32_t box_rows) {
+  return encode_map(m, base, rows, cols, 64, box_rows, CU_TENSOR_MAP_SWIZZLE_128B);
+}
+// epilogue stores: 32 x 32 blocks, 64-byte swizzle (matches EpiStore's shared-memory layout)
+static bool make_store_map(CUtensorMap *m, const void *base, uint64_t rows, uint64_t cols) {
+  return encode_map(m, base, rows, cols, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B);
+}
 
+constexpr uint32_t MN_BOX = P_BK;   // k rows of an MN-major TMA box (both kernels take P_BK == BK)
+static_assert(P_BK == BK, "the single-CTA and pair kernels share the MN-major tensor maps");
+
+// The pair kernel pairs two row tiles of one expert, so an expert with an odd number of row tiles
+// computes one tile it throws away; with few row tiles per expert the single-CTA kernel wins.
+static bool use_pair(int kind, int64_t rows_max, int E) {
+  if (kind == WGRAD) return true;   // pairs along the weight rows: no waste
+  return rows_max / BM >= 4 * (int64_t)E;
+}
+
+// max_tiles / max_pair_tiles: host upper bounds on the tile counts (the exact counts live on the device)
 template <int KIND>
-static int launch(const CUtensorMap &a, const CUtensorMap &b, const Params &p, int64_t max_tiles, cudaStream_t s) {
+static int launch(const CUtensorMap &a, const CUtensorMap &b, const CUtensorMap &c0, const CUtensorMap &c1,
+                  const Params &p, int64_t max_tiles, int64_t max_pair_tiles, bool pair, cudaStream_t s) {
+  if (pair) {
+    MOE_TRY_CUDA(cudaFuncSetAttribute(tc_pair_kernel<KIND>, cudaFuncAttributeMaxDynamicSharedMemorySize, P_SMEM_BYTES));
+    int64_t clusters = sm_count() / 2;
+    if (max_pair_tiles < clusters) clusters = max_pair_tiles;
+    if (clusters < 1) clusters = 1;
+    tc_pair_kernel<KIND><<<(int)(2 * clusters), THREADS, P_SMEM_BYTES, s>>>(a, b, c0, c1, p);
+    MOE_CHECK_LAUNCH();
+    return MOE_OK;
+  }
   MOE_TRY_CUDA(cudaFuncSetAttribute(tc_gemm_kernel<KIND>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES));
   int64_t grid = sm_count();
   if (max_tiles < grid) grid = max_tiles;
   if (grid < 1) grid = 1;
-  tc_gemm_kernel<KIND><<<(int)grid, THREADS, SMEM_BYTES, s>>>(a, b, p);
+  tc_gemm_kernel<KIND><<<(int)grid, THREADS, SMEM_BYTES, s>>>(a, b, c0, c1, p);
   MOE_CHECK_LAUNCH();
   return MOE_OK;
 }
@@ -503,7 +776,7 @@ static int launch(const CUtensorMap &a, const CUtensorMap &b, const Params &p, i
 int tc_grouped_ffn_fwd(const void *x_perm, const void *wgu, const void *wd, const int32_t *tile_offsets, int E, int d,
                        int f, int64_t rows_max, void *ab, void *h, void *y, WsHeader *hdr, cudaStream_t s) {
   using namespace tc;
-  CUtensorMap mA, mB;
+  CUtensorMap mA, mB, mC0, mC1;
   Params p{};
   p.tile_offsets = tile_offsets;
   p.hdr = hdr;
@@ -511,8 +784,10 @@ int tc_grouped_ffn_fwd(const void *x_perm, const void *wgu, const void *wd, cons
   p.d = d;
   p.f = f;
   const int64_t row_tiles = rows_max / BM;
+  const int64_t pair_rows = (row_tiles + 1) / 2 + E;   // upper bound on pair rows (one odd tile per expert)
   // GEMM1: [a | b] = x_perm Wgu^T, SwiGLU epilogue
-  if (!make_map(&mA, x_perm, rows_max, d, 128) || !make_map(&mB, wgu, (uint64_t)E * 2 * f, d, 128))
+  if (!make_map(&mA, x_perm, rows_max, d, 128) || !make_map(&mB, wgu, (uint64_t)E * 2 * f, d, 128) ||
+      !make_store_map(&mC0, ab, rows_max, 2 * f) || !make_store_map(&mC1, h, rows_max, f))
     return MOE_ERR_CUDA;
   p.n_tiles = f / (BN / 2);
   p.num_kb = d / BK;
@@ -521,24 +796,28 @@ int tc_grouped_ffn_fwd(const void *x_perm, const void *wgu, const void *wd, cons
   p.ld0 = 2 * (int64_t)f;
   p.out1 = (__nv_bfloat16 *)h;
   p.ld1 = f;
-  int rc = launch<GATEUP>(mA, mB, p, row_tiles * p.n_tiles, s);
+  int rc = launch<GATEUP>(mA, mB, mC0, mC1, p, row_tiles * p.n_tiles, pair_rows * p.n_tiles,
+                          use_pair(GATEUP, rows_max, E), s);
   if (rc) return rc;
   // GEMM2: y = h Wd^T
-  if (!make_map(&mA, h, rows_max, f, 128) || !make_map(&mB, wd, (uint64_t)E * d, f, 128)) return MOE_ERR_CUDA;
+  if (!make_map(&mA, h, rows_max, f, 128) || !make_map(&mB, wd, (uint64_t)E * d, f, 128) ||
+      !make_store_map(&mC0, y, rows_max, d))
+    return MOE_ERR_CUDA;
   p.n_tiles = d / BN;
   p.num_kb = f / BK;
   p.b_rows_e = d;
   p.out0 = (__nv_bfloat16 *)y;
   p.ld0 = d;
   p.out1 = nullptr;
-  return launch<DOWN>(mA, mB, p, row_tiles * p.n_tiles, s);
+  return launch<DOWN>(mA, mB, mC0, mC0, p, row_tiles * p.n_tiles, pair_rows * p.n_tiles, use_pair(DOWN, rows_max, E),
+                      s);
 }
 
 int tc_grouped_ffn_bwd(const void *dy, const void *x_perm, const void *ab, const void *h, const void *wgu,
                        const void *wd, const int32_t *tile_offsets, int E, int d, int f, int64_t rows_max, void *dab,
                        void *dx, void *dwgu, void *dwd, WsHeader *hdr, cudaStream_t s) {
   using namespace tc;
-  CUtensorMap mA, mB;
+  CUtensorMap mA, mB, mC;
   Params p{};
   p.tile_offsets = tile_offsets;
   p.hdr = hdr;
@@ -546,9 +825,12 @@ int tc_grouped_ffn_bwd(const void *dy, const void *x_perm, const void *ab, const
   p.d = d;
   p.f = f;
   const int64_t row_tiles = rows_max / BM;
+  const int64_t pair_rows = (row_tiles + 1) / 2 + E;
   int rc;
   // dh = dy Wd[e] (Wd read MN-major), SwiGLU backward epilogue -> dab
-  if (!make_map(&mA, dy, rows_max, d, 128) || !make_map(&mB, wd, (uint64_t)E * d, f, 64)) return MOE_ERR_CUDA;
+  if (!make_map(&mA, dy, rows_max, d, 128) || !make_map(&mB, wd, (uint64_t)E * d, f, MN_BOX) ||
+      !make_store_map(&mC, dab, rows_max, 2 * f))
+    return MOE_ERR_CUDA;
   p.n_tiles = f / BN;
   p.num_kb = d / BK;
   p.b_rows_e = d;
@@ -556,33 +838,44 @@ int tc_grouped_ffn_bwd(const void *dy, const void *x_perm, const void *ab, const
   p.ld0 = 2 * (int64_t)f;
   p.aux = (const __nv_bfloat16 *)ab;
   p.ld_aux = 2 * (int64_t)f;
-  if ((rc = launch<DH>(mA, mB, p, row_tiles * p.n_tiles, s))) return rc;
+  if ((rc = launch<DH>(mA, mB, mC, mC, p, row_tiles * p.n_tiles, pair_rows * p.n_tiles, use_pair(DH, rows_max, E), s)))
+    return rc;
   // dWd[e] = dy_e^T h_e
-  if (!make_map(&mA, dy, rows_max, d, 64) || !make_map(&mB, h, rows_max, f, 64)) return MOE_ERR_CUDA;
+  if (!make_map(&mA, dy, rows_max, d, MN_BOX) || !make_map(&mB, h, rows_max, f, MN_BOX) ||
+      !make_store_map(&mC, dwd, (uint64_t)E * d, f))
+    return MOE_ERR_CUDA;
   p.m_tiles = d / BM;
   p.n_tiles = f / BN;
   p.out0 = (__nv_bfloat16 *)dwd;
   p.ld0 = f;
   p.out_e_stride = (int64_t)d * f;
   p.aux = nullptr;
-  if ((rc = launch<WGRAD>(mA, mB, p, (int64_t)E * p.m_tiles * p.n_tiles, s))) return rc;
+  if ((rc = launch<WGRAD>(mA, mB, mC, mC, p, (int64_t)E * p.m_tiles * p.n_tiles,
+                          (int64_t)E * (p.m_tiles / 2) * p.n_tiles, use_pair(WGRAD, rows_max, E), s)))
+    return rc;
   // dx_perm = dab Wgu[e] (Wgu read MN-major)
-  if (!make_map(&mA, dab, rows_max, 2 * f, 128) || !make_map(&mB, wgu, (uint64_t)E * 2 * f, d, 64))
+  if (!make_map(&mA, dab, rows_max, 2 * f, 128) || !make_map(&mB, wgu, (uint64_t)E * 2 * f, d, MN_BOX) ||
+      !make_store_map(&mC, dx, rows_max, d))
     return MOE_ERR_CUDA;
   p.n_tiles = d / BN;
   p.num_kb = 2 * f / BK;
   p.b_rows_e = 2 * f;
   p.out0 = (__nv_bfloat16 *)dx;
   p.ld0 = d;
-  if ((rc = launch<DGRAD>(mA, mB, p, row_tiles * p.n_tiles, s))) return rc;
+  if ((rc = launch<DGRAD>(mA, mB, mC, mC, p, row_tiles * p.n_tiles, pair_rows * p.n_tiles,
+                          use_pair(DGRAD, rows_max, E), s)))
+    return rc;
   // dWgu[e] = dab_e^T x_perm_e
-  if (!make_map(&mA, dab, rows_max, 2 * f, 64) || !make_map(&mB, x_perm, rows_max, d, 64)) return MOE_ERR_CUDA;
+  if (!make_map(&mA, dab, rows_max, 2 * f, MN_BOX) || !make_map(&mB, x_perm, rows_max, d, MN_BOX) ||
+      !make_store_map(&mC, dwgu, (uint64_t)E * 2 * f, d))
+    return MOE_ERR_CUDA;
   p.m_tiles = 2 * f / BM;
   p.n_tiles = d / BN;
   p.out0 = (__nv_bfloat16 *)dwgu;
   p.ld0 = d;
   p.out_e_stride = (int64_t)2 * f * d;
-  return launch<WGRAD>(mA, mB, p, (int64_t)E * p.m_tiles * p.n_tiles, s);
+  return launch<WGRAD>(mA, mB, mC, mC, p, (int64_t)E * p.m_tiles * p.n_tiles, (int64_t)E * (p.m_tiles / 2) * p.n_tiles,
+                       use_pair(WGRAD, rows_max, E), s);
 }
 
 }  // namespace moe

@@ -13,18 +13,28 @@ from helpers import grouped_rows, rel_err, tile_offsets_from_counts, tol_for
 pytestmark = pytest.mark.gpu
 
 CASES = [
-    # E, d, f, counts (ragged, empty, a single row, exact multiples of the tile)
-    (4, 512, 512, [300, 0, 129, 1]),
-    (3, 256, 256, [128, 256, 5]),
-    (2, 256, 768, [1, 383]),
+    # E, d, f, counts (ragged, empty, a single row, exact multiples of the tile), kernel path. With
+    # fewer than 4 row tiles per expert on average (rows_max / 128 < 4 E) the row-grouped kinds run
+    # on the single-CTA kernel, otherwise on the CTA-pair kernel (odd tile counts leave a half-used
+    # last pair). The weight-gradient kind always runs on the pair kernel.
+    (4, 512, 512, [300, 0, 129, 1], "single"),
+    (3, 256, 256, [128, 256, 5], "single"),
+    (2, 256, 768, [1, 383], "single"),
+    (4, 512, 512, [300, 0, 129, 1], "pair"),
+    (2, 512, 512, [700, 1000], "pair"),
+    (3, 256, 512, [1100, 0, 513], "pair"),
+    (4, 512, 256, [1024, 1, 640, 897], "pair"),
 ]
 
 
-def _setup(E, d, f, counts, dtype, seed=0):
+def _setup(E, d, f, counts, dtype, path, seed=0):
     from mixture_experts_layer_histogram_gb300 import _lib as L
     g = torch.Generator().manual_seed(seed)
     toff = tile_offsets_from_counts(counts)
     R = toff[-1] * 128 + 256          # a few unused rows after the last group
+    if path == "pair":                 # the kernel choice follows rows_max / (128 E), as in a real layer
+        R = max(R, 4 * 128 * E)
+    assert (R // 128 >= 4 * E) == (path == "pair")
     rows = grouped_rows(counts)
     real = torch.zeros(R, dtype=torch.bool)
     for rr in rows:
@@ -48,9 +58,9 @@ def _setup(E, d, f, counts, dtype, seed=0):
 
 
 @pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
-@pytest.mark.parametrize("E,d,f,counts", CASES)
-def test_grouped_gemm_kinds(E, d, f, counts, dtype):
-    L, t, gt, rows, ws, o = _setup(E, d, f, counts, dtype)
+@pytest.mark.parametrize("E,d,f,counts,path", CASES)
+def test_grouped_gemm_kinds(E, d, f, counts, path, dtype):
+    L, t, gt, rows, ws, o = _setup(E, d, f, counts, dtype, path)
     L.moe_grouped_ffn_fwd(gt["x"], gt["wgu"], gt["wd"], gt["toff"], o["ab"], o["h"], o["y"], ws)
     L.moe_grouped_ffn_bwd(gt["dy"], gt["x"], o["ab"], o["h"], gt["wgu"], gt["wd"], gt["toff"], o["dab"], o["dx"],
                           o["dwgu"], o["dwd"], ws)
