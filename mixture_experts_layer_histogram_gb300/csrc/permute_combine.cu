@@ -118,7 +118,8 @@ __global__ void __launch_bounds__(kRowThreads) combine_kernel(const uint4 *__res
 }
 
 // ---------------------------------------------------------------------------------------------
-template <typename T>
+// KMAX: compile-time upper bound on k (the per-slot arrays live in registers)
+template <typename T, int KMAX>
 __global__ void __launch_bounds__(kRowThreads) combine_bwd_kernel(
     const uint4 *__restrict__ g, const uint4 *__restrict__ y, const float *__restrict__ w,
     const int32_t *__restrict__ topk_idx, const int32_t *__restrict__ row_of_slot, const int32_t *__restrict__ counts,
@@ -135,37 +136,48 @@ __global__ void __launch_bounds__(kRowThreads) combine_bwd_kernel(
     const int myrow = load_row(row_of_slot, t, k, lane, rows_max);
     const float myw = lane < k ? __ldg(w + t * k + lane) : 0.0f;
     const int mye = lane < k ? __ldg(topk_idx + t * k + lane) : -1;
-    float part[MOE_MAX_TOPK];
+    float part[KMAX];
 #pragma unroll
-    for (int j = 0; j < MOE_MAX_TOPK; ++j) part[j] = 0.0f;
-    // warp-uniform loop: every lane reaches every shuffle; loads and stores are predicated
+    for (int j = 0; j < KMAX; ++j) part[j] = 0.0f;
+    int rows[KMAX];
+    float ws[KMAX];
+#pragma unroll
+    for (int j = 0; j < KMAX; ++j) {
+      rows[j] = j < k ? __shfl_sync(0xffffffffu, myrow, j) : -1;
+      ws[j] = j < k ? __shfl_sync(0xffffffffu, myw, j) : 0.0f;
+    }
+    // warp-uniform loop over 512-byte chunks of the row; per chunk all k expert rows are loaded
+    // before any dy row is stored, so the k loads are in flight together
     for (int64_t v0 = 0; v0 < row_vecs; v0 += 32) {
       const int64_t v = v0 + lane;
       const bool act = v < row_vecs;
-      float gv[N];
-      if (act) Elem<T>::unpack(ld_stream(g + t * row_vecs + v), gv);
+      uint4 gq = make_uint4(0, 0, 0, 0), yq[KMAX];
+      if (act) gq = ld_stream(g + t * row_vecs + v);
 #pragma unroll
-      for (int j = 0; j < MOE_MAX_TOPK; ++j) {
+      for (int j = 0; j < KMAX; ++j)
+        if (j < k && act && rows[j] >= 0) yq[j] = ld_stream(y + (int64_t)rows[j] * row_vecs + v);
+      float gv[N];
+      Elem<T>::unpack(gq, gv);
+#pragma unroll
+      for (int j = 0; j < KMAX; ++j) {
         if (j >= k) break;
-        int r = __shfl_sync(0xffffffffu, myrow, j);
-        float wj = __shfl_sync(0xffffffffu, myw, j);
-        if (r < 0 || !act) continue;
+        if (!act || rows[j] < 0) continue;
         float yv[N], o[N];
-        Elem<T>::unpack(ld_stream(y + (int64_t)r * row_vecs + v), yv);
+        Elem<T>::unpack(yq[j], yv);
         float s = 0.0f;
 #pragma unroll
         for (int i = 0; i < N; ++i) {
           s = fmaf(gv[i], yv[i], s);
-          o[i] = wj * gv[i];
+          o[i] = ws[j] * gv[i];
         }
         part[j] += s;
-        dy[(int64_t)r * row_vecs + v] = Elem<T>::pack(o);
+        dy[(int64_t)rows[j] * row_vecs + v] = Elem<T>::pack(o);
       }
     }
     // d_topk_w[t, j] = <g, y_j>: reduce each partial over the warp; lane j keeps slot j
     float dw = 0.0f;
 #pragma unroll
-    for (int j = 0; j < MOE_MAX_TOPK; ++j) {
+    for (int j = 0; j < KMAX; ++j) {
       if (j >= k) break;
       float s = part[j];
 #pragma unroll
@@ -261,14 +273,22 @@ extern "C" int moe_combine_bwd(const void *grad_out, const void *y_perm, const f
   const int64_t rv = (int64_t)(row_bytes / 16);
   const int tb = row_blocks(T);
   cudaStream_t s = (cudaStream_t)stream;
-  if (dtype == MOE_BF16)
-    combine_bwd_kernel<__nv_bfloat16><<<tb + E, kRowThreads, 0, s>>>(
-        (const uint4 *)grad_out, (const uint4 *)y_perm, topk_w, topk_idx, row_of_slot, counts, tile_offsets,
-        MOE_GROUP_ROWS, T, rv, k, E, rows_max, tb, (uint4 *)dy_perm, d_topk_w, d_logits);
-  else
-    combine_bwd_kernel<float><<<tb + E, kRowThreads, 0, s>>>(
-        (const uint4 *)grad_out, (const uint4 *)y_perm, topk_w, topk_idx, row_of_slot, counts, tile_offsets,
-        MOE_GROUP_ROWS, T, rv, k, E, rows_max, tb, (uint4 *)dy_perm, d_topk_w, d_logits);
+#define MOE_COMBINE_BWD(TYPE, KM)                                                                               \
+  combine_bwd_kernel<TYPE, KM><<<tb + E, kRowThreads, 0, s>>>(                                                  \
+      (const uint4 *)grad_out, (const uint4 *)y_perm, topk_w, topk_idx, row_of_slot, counts, tile_offsets,     \
+      MOE_GROUP_ROWS, T, rv, k, E, rows_max, tb, (uint4 *)dy_perm, d_topk_w, d_logits)
+  if (dtype == MOE_BF16) {
+    if (k <= 2) MOE_COMBINE_BWD(__nv_bfloat16, 2);
+    else if (k <= 4) MOE_COMBINE_BWD(__nv_bfloat16, 4);
+    else if (k <= 8) MOE_COMBINE_BWD(__nv_bfloat16, 8);
+    else MOE_COMBINE_BWD(__nv_bfloat16, 16);
+  } else {
+    if (k <= 2) MOE_COMBINE_BWD(float, 2);
+    else if (k <= 4) MOE_COMBINE_BWD(float, 4);
+    else if (k <= 8) MOE_COMBINE_BWD(float, 8);
+    else MOE_COMBINE_BWD(float, 16);
+  }
+#undef MOE_COMBINE_BWD
   MOE_CHECK_LAUNCH();
   return MOE_OK;
 }
