@@ -428,8 +428,16 @@ constexpr int P_STAGES = 6;
 constexpr int P_A_BYTES = BM * P_BK * 2;        // this CTA's 128 rows of A
 constexpr int P_B_BYTES = (BN / 2) * P_BK * 2;  // this CTA's half of B
 constexpr int P_STAGE_BYTES = P_A_BYTES + P_B_BYTES;
-constexpr int P_SMEM_BYTES = P_STAGES * P_STAGE_BYTES + EPI_STAGE_BYTES + 1024 + 160 + (MAX_E + 1) * 4;
-static_assert(P_SMEM_BYTES <= 232448, "pair kernel shared memory exceeds 227 KB");
+// Per-kind layout: the DH kind gives one ring stage to per-warp buffers that bring the saved a, b
+// blocks in by TMA (two 4 KB buffers per epilogue warp, filled two 32-column chunks ahead).
+constexpr int DH_BUF_BYTES = 2 * EPI_BUF_BYTES;   // a block + b block of one chunk
+template <int KIND> struct PairCfg {
+  static constexpr int STAGES = KIND == DH ? P_STAGES - 1 : P_STAGES;
+  static constexpr int EPI_BYTES = KIND == DH ? EPI_WARPS * 2 * DH_BUF_BYTES : EPI_STAGE_BYTES;
+  static constexpr int NBARS = 2 * STAGES + 5 + (KIND == DH ? 2 * EPI_WARPS : 0);
+  static constexpr int SMEM = STAGES * P_STAGE_BYTES + EPI_BYTES + 1024 + 8 * NBARS + 16 + (MAX_E + 1) * 4;
+  static_assert(SMEM <= 232448, "pair kernel shared memory exceeds 227 KB");
+};
 
 // Instruction descriptor for the pair MMA: M = 256 (128 rows per CTA), N = 256.
 __host__ __device__ constexpr uint32_t idesc_bf16_pair(bool a_mn, bool b_mn) {
@@ -477,12 +485,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
                    const __grid_constant__ CUtensorMap tmC0, const __grid_constant__ CUtensorMap tmC1, const Params p) {
   constexpr bool A_MN = (KIND == WGRAD);
   constexpr bool B_MN = (KIND == DH || KIND == DGRAD || KIND == WGRAD);
+  constexpr int PS = PairCfg<KIND>::STAGES;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t *epi_smem = smem + P_STAGES * P_STAGE_BYTES;
-  uint64_t *bars = reinterpret_cast<uint64_t *>(epi_smem + EPI_STAGE_BYTES);
-  // bars: full[P_STAGES], empty[P_STAGES], tfull[2], tempty[2], mma_done
-  uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(bars + 2 * P_STAGES + 5);
+  uint8_t *epi_smem = smem + PS * P_STAGE_BYTES;
+  uint64_t *bars = reinterpret_cast<uint64_t *>(epi_smem + PairCfg<KIND>::EPI_BYTES);
+  // bars: full[PS], empty[PS], tfull[2], tempty[2], mma_done, (DH) two load barriers per epilogue warp
+  uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(bars + PairCfg<KIND>::NBARS);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_holder + 1);
   int *ptoff = reinterpret_cast<int *>(tmem_holder + 4);
   const int *toff = p.tile_offsets;   // read through L1; shared memory goes to the ring
@@ -493,13 +502,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
   const uint32_t sbase = smem_u32(smem);
   const uint32_t bar0 = smem_u32(bars);
   auto full_bar = [&](int s) { return bar0 + 8u * s; };
-  auto empty_bar = [&](int s) { return bar0 + 8u * (P_STAGES + s); };
-  auto tfull_bar = [&](int a) { return bar0 + 8u * (2 * P_STAGES + a); };
-  auto tempty_bar = [&](int a) { return bar0 + 8u * (2 * P_STAGES + 2 + a); };
-  const uint32_t mma_done_bar = bar0 + 8u * (2 * P_STAGES + 4);
+  auto empty_bar = [&](int s) { return bar0 + 8u * (PS + s); };
+  auto tfull_bar = [&](int a) { return bar0 + 8u * (2 * PS + a); };
+  auto tempty_bar = [&](int a) { return bar0 + 8u * (2 * PS + 2 + a); };
+  const uint32_t mma_done_bar = bar0 + 8u * (2 * PS + 4);
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < P_STAGES; ++s) {
+    for (int s = 0; s < PS; ++s) {
       mbar_init(full_bar(s), 1);
       mbar_init(empty_bar(s), 1);
     }
@@ -508,6 +517,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
       mbar_init(tempty_bar(a), 2 * EPI_WARPS);   // one arrival per epilogue warp of both CTAs
     }
     mbar_init(mma_done_bar, 1);
+    if (KIND == DH)
+      for (int i = 0; i < 2 * EPI_WARPS; ++i) mbar_init(bar0 + 8u * (2 * PS + 5 + i), 1);
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmA)) : "memory");
@@ -589,7 +600,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
         const uint32_t fb = mapa_shared(full_bar(stage), 0);   // the leader's full barrier
         if (leader) mbar_expect_tx(full_bar(stage), 2 * P_STAGE_BYTES);
         boxes(t, kb, sA, sB, fb);
-        if (++stage == P_STAGES) { stage = 0; phase ^= 1u; }
+        if (++stage == PS) { stage = 0; phase ^= 1u; }
       }
       if (!ok) break;
     }
@@ -622,7 +633,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
         }
         issued_any = true;
         mma_commit_pair(empty_bar(stage), 0x3);   // frees this stage in both CTAs
-        if (++stage == P_STAGES) { stage = 0; phase ^= 1u; }
+        if (++stage == PS) { stage = 0; phase ^= 1u; }
       }
       if (!ok) break;
       mma_commit_pair(tfull_bar(acc), 0x3);       // both CTAs' accumulators are ready
@@ -634,6 +645,112 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
       const uint64_t t0 = global_ns();
       while (!mbar_try_wait(mma_done_bar, 0) && global_ns() - t0 < kWaitLimitNs) {}
     }
+  } else if (warp >= 2 && KIND == DH) {
+    // ------------------------------------------------------------------ DH epilogue (both CTAs)
+    // Per warp: its 32 rows x one 128-column half of the tile, in four 32-column chunks. The saved
+    // a and b blocks of a chunk arrive by TMA (tmC1 = ab) into one of two 4 KB buffers two chunks
+    // ahead of use (across tiles); da and db are written back in place and stored by TMA (tmC0 = dab).
+    const int quarter = warp & 3;
+    const int half = (warp - 2) >> 2;
+    const int c0 = half * (BN / 2);
+    const uint32_t dbuf = smem_u32(epi_smem) + (uint32_t)(warp - 2) * 2 * DH_BUF_BYTES;
+    const uint32_t lbar = bar0 + 8u * (2 * PS + 5 + 2 * (warp - 2));
+    uint32_t lphase = 0;   // bit b: parity of buffer b's next fill
+    // load cursor: next (tile, chunk) to bring in
+    int ltile = cluster_id, lj = 0;
+    auto issue_load = [&](int bi) {
+      if (ltile >= num_tiles) return;
+      bool lv;
+      const Tile lt = decode_pair<KIND>(ltile, p, toff, ptoff, (int)rank, lv);
+      if (lane == 0) {
+        asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");   // the buffer's last store has read it
+        const uint32_t b = dbuf + (uint32_t)bi * DH_BUF_BYTES, bar = lbar + 8u * bi;
+        const int x = lt.n0 + c0 + 32 * lj, y = lt.m0 + quarter * 32;
+        mbar_expect_tx(bar, DH_BUF_BYTES);
+        tma_load_2d(b, &tmC1, x, y, bar);
+        tma_load_2d(b + EPI_BUF_BYTES, &tmC1, p.f + x, y, bar);
+      }
+      if (++lj == 4) { lj = 0; ltile += num_clusters; }
+    };
+    issue_load(0);
+    issue_load(1);
+    int acc = 0, bi = 0;
+    uint32_t acc_phase = 0;
+    const uint32_t sw = (uint32_t)(lane >> 1) & 3u;
+    for (int tile = cluster_id; tile < num_tiles; tile += num_clusters) {
+      bool valid;
+      const Tile t = decode_pair<KIND>(tile, p, toff, ptoff, (int)rank, valid);
+      if (!mbar_wait_cluster(tfull_bar(acc), acc_phase, abort_flag, p.hdr, 14)) break;
+      tc_fence_after();
+      const uint32_t tbase = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * BN);
+      const int yrow = t.m0 + quarter * 32;
+      bool ok = true;
+#pragma unroll 1
+      for (int j = 0; j < 4; ++j) {
+        const int c = c0 + 32 * j;
+        uint32_t r[32];
+        tmem_ld32(tbase + c, r);
+        if (!mbar_wait_cluster(lbar + 8u * bi, (lphase >> bi) & 1u, abort_flag, p.hdr, 17)) { ok = false; break; }
+        lphase ^= 1u << bi;
+        const uint32_t ra = dbuf + (uint32_t)bi * DH_BUF_BYTES + (uint32_t)lane * 64, rb = ra + EPI_BUF_BYTES;
+        float av[32], bv[32];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          uint4 qa, qb;
+          const uint32_t off = (uint32_t)(q ^ sw) << 4;
+          asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];" : "=r"(qa.x), "=r"(qa.y), "=r"(qa.z), "=r"(qa.w)
+                       : "r"(ra + off));
+          asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];" : "=r"(qb.x), "=r"(qb.y), "=r"(qb.z), "=r"(qb.w)
+                       : "r"(rb + off));
+          unpack_bf16x8(qa, av + 8 * q);
+          unpack_bf16x8(qb, bv + 8 * q);
+        }
+        tmem_ld_wait();
+        float da[32], db[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          const float dh = __uint_as_float(r[i]), a = av[i], sg = sigmoidf_(a);
+          da[i] = dh * bv[i] * sg * (1.0f + a * (1.0f - sg));
+          db[i] = dh * a * sg;
+        }
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const uint32_t off = (uint32_t)(q ^ sw) << 4;
+          const uint4 qa = pack_bf16x8(da + 8 * q), qb = pack_bf16x8(db + 8 * q);
+          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(ra + off), "r"(qa.x), "r"(qa.y), "r"(qa.z),
+                       "r"(qa.w)
+                       : "memory");
+          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(rb + off), "r"(qb.x), "r"(qb.y), "r"(qb.z),
+                       "r"(qb.w)
+                       : "memory");
+        }
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        __syncwarp();
+        if (valid && lane == 0) {
+          const uint32_t b = dbuf + (uint32_t)bi * DH_BUF_BYTES;
+          asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
+                           reinterpret_cast<uint64_t>(&tmC0)),
+                       "r"(t.n0 + c), "r"(yrow), "r"(b)
+                       : "memory");
+          asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
+                           reinterpret_cast<uint64_t>(&tmC0)),
+                       "r"(p.f + t.n0 + c), "r"(yrow), "r"(b + EPI_BUF_BYTES)
+                       : "memory");
+          asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+        }
+        issue_load(bi);   // the chunk two ahead reuses this buffer once its store has read it
+        __syncwarp();
+        bi ^= 1;
+      }
+      if (!ok) break;
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster(mapa_shared(tempty_bar(acc), 0));
+      acc ^= 1;
+      if (acc == 0) acc_phase ^= 1u;
+    }
+    if (lane == 0) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+    __syncwarp();
   } else if (warp >= 2) {
     // ------------------------------------------------------------------ epilogue (both CTAs)
     const int quarter = warp & 3;
@@ -753,11 +870,22 @@ template <int KIND>
 static int launch(const CUtensorMap &a, const CUtensorMap &b, const CUtensorMap &c0, const CUtensorMap &c1,
                   const Params &p, int64_t max_tiles, int64_t max_pair_tiles, bool pair, cudaStream_t s) {
   if (pair) {
-    MOE_TRY_CUDA(cudaFuncSetAttribute(tc_pair_kernel<KIND>, cudaFuncAttributeMaxDynamicSharedMemorySize, P_SMEM_BYTES));
-    int64_t clusters = sm_count() / 2;
+    constexpr int smem = PairCfg<KIND>::SMEM;
+    MOE_TRY_CUDA(cudaFuncSetAttribute(tc_pair_kernel<KIND>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem));
+    // a persistent grid must fit at once: launch only as many pairs as can be co-resident
+    int resident = 0;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(sm_count() / 2 * 2), 1, 1);
+    cfg.blockDim = dim3(THREADS, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    if (cudaOccupancyMaxActiveClusters(&resident, tc_pair_kernel<KIND>, &cfg) != cudaSuccess || resident < 1) {
+      (void)cudaGetLastError();
+      resident = sm_count() / 2;
+    }
+    int64_t clusters = resident;
     if (max_pair_tiles < clusters) clusters = max_pair_tiles;
     if (clusters < 1) clusters = 1;
-    tc_pair_kernel<KIND><<<(int)(2 * clusters), THREADS, P_SMEM_BYTES, s>>>(a, b, c0, c1, p);
+    tc_pair_kernel<KIND><<<(int)(2 * clusters), THREADS, smem, s>>>(a, b, c0, c1, p);
     MOE_CHECK_LAUNCH();
     return MOE_OK;
   }
@@ -828,8 +956,9 @@ int tc_grouped_ffn_bwd(const void *dy, const void *x_perm, const void *ab, const
   const int64_t pair_rows = (row_tiles + 1) / 2 + E;
   int rc;
   // dh = dy Wd[e] (Wd read MN-major), SwiGLU backward epilogue -> dab
+  CUtensorMap mAB;   // the saved a, b blocks, read by the pair kernel's DH epilogue
   if (!make_map(&mA, dy, rows_max, d, 128) || !make_map(&mB, wd, (uint64_t)E * d, f, MN_BOX) ||
-      !make_store_map(&mC, dab, rows_max, 2 * f))
+      !make_store_map(&mC, dab, rows_max, 2 * f) || !make_store_map(&mAB, ab, rows_max, 2 * f))
     return MOE_ERR_CUDA;
   p.n_tiles = f / BN;
   p.num_kb = d / BK;
@@ -838,7 +967,7 @@ int tc_grouped_ffn_bwd(const void *dy, const void *x_perm, const void *ab, const
   p.ld0 = 2 * (int64_t)f;
   p.aux = (const __nv_bfloat16 *)ab;
   p.ld_aux = 2 * (int64_t)f;
-  if ((rc = launch<DH>(mA, mB, mC, mC, p, row_tiles * p.n_tiles, pair_rows * p.n_tiles, use_pair(DH, rows_max, E), s)))
+  if ((rc = launch<DH>(mA, mB, mC, mAB, p, row_tiles * p.n_tiles, pair_rows * p.n_tiles, use_pair(DH, rows_max, E), s)))
     return rc;
   // dWd[e] = dy_e^T h_e
   if (!make_map(&mA, dy, rows_max, d, MN_BOX) || !make_map(&mB, h, rows_max, f, MN_BOX) ||
