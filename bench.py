@@ -28,6 +28,10 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "MoE layer fwd+bwd tokens/s (E=64,k=8,d=2048); grouped-GEMM % BF16 peak"
+
+# DRAM bytes (read + write) of the grouped-GEMM launches of one step, from an ncu capture of the
+# current kernels (profiles/dram_fwdbwd_t8192.md); None where no capture of the current kernels exists.
+GEMM_TRAFFIC = {"fwdbwd_t8192": 5797000000}
 DEFAULT_WORKLOAD = "fwdbwd_t8192"
 
 
@@ -125,18 +129,20 @@ def run_ours(args):
     dev = torch.device("cuda", local if world > 1 else 0)
     torch.cuda.set_device(dev)
     w = moe_inputs.WORKLOADS[args.workload]
-    assert w.backward, "the bench times forward + backward"
     inp = moe_inputs.make_all(w, dev)
-    x, logits, wgu, wd, g = inp["x"], inp["logits"], inp["w_gate_up"], inp["w_down"], inp["g"]
-    layer = MoELayer(w.T, w.d, w.E, w.k, w.f, w.torch_dtype, dev)
+    x, logits, wgu, wd = inp["x"], inp["logits"], inp["w_gate_up"], inp["w_down"]
+    g = inp.get("g")
+    bwd = w.backward
+    layer = MoELayer(w.T, w.d, w.E, w.k, w.f, w.torch_dtype, dev, backward=bwd)
     stream = torch.cuda.current_stream(dev)
     M = w.T * w.k
-    gemm_flop = 18.0 * M * w.d * w.f
+    gemm_flop = (18.0 if bwd else 6.0) * M * w.d * w.f
 
     def step(ev=None):
         if ev is None:
             layer.forward(x, logits, wgu, wd)
-            layer.backward(g, wgu, wd)
+            if bwd:
+                layer.backward(g, wgu, wd)
             return
         # events around each C-ABI call, on the stream the kernels are launched on
         ev[0].record(stream)
@@ -152,6 +158,11 @@ def run_ours(args):
         ev[4].record(stream)
         L.moe_combine_fwd(layer.y_perm, layer.topk_w, layer.row_of_slot, w.T, w.k, layer.out)
         ev[5].record(stream)
+        if not bwd:
+            ev[6].record(stream)
+            ev[7].record(stream)
+            ev[8].record(stream)
+            return
         L.moe_combine_bwd(g, layer.y_perm, layer.topk_w, layer.topk_idx, layer.row_of_slot, layer.counts,
                           layer.tile_offsets, w.E, layer.dy_perm, layer.d_topk_w, layer.d_logits)
         ev[6].record(stream)
@@ -198,22 +209,26 @@ def run_ours(args):
         raise RuntimeError(f"device status after timing: {st}")
 
     # ---------------------------------------------------------------- end to end: host buffers
-    pin = dict(x=x.cpu().pin_memory(), logits=logits.cpu().pin_memory(), g=g.cpu().pin_memory())
-    host_out = {k: torch.empty(v.shape, dtype=v.dtype).pin_memory()
-                for k, v in (("out", layer.out), ("dx", layer.dx), ("d_logits", layer.d_logits))}
-    dx_, dl_, dg_ = torch.empty_like(x), torch.empty_like(logits), torch.empty_like(g)
+    pin = dict(x=x.cpu().pin_memory(), logits=logits.cpu().pin_memory())
+    results = [("out", layer.out)]
+    if bwd:
+        pin["g"] = g.cpu().pin_memory()
+        results += [("dx", layer.dx), ("d_logits", layer.d_logits)]
+    host_out = {k: torch.empty(v.shape, dtype=v.dtype).pin_memory() for k, v in results}
+    dx_, dl_ = torch.empty_like(x), torch.empty_like(logits)
+    dg_ = torch.empty_like(g) if bwd else None
     h2d = sum(v.numel() * v.element_size() for v in pin.values())
     d2h = sum(v.numel() * v.element_size() for v in host_out.values())
 
     def e2e_step():
         dx_.copy_(pin["x"], non_blocking=True)
         dl_.copy_(pin["logits"], non_blocking=True)
-        dg_.copy_(pin["g"], non_blocking=True)
         layer.forward(dx_, dl_, wgu, wd)
-        layer.backward(dg_, wgu, wd)
-        host_out["out"].copy_(layer.out, non_blocking=True)
-        host_out["dx"].copy_(layer.dx, non_blocking=True)
-        host_out["d_logits"].copy_(layer.d_logits, non_blocking=True)
+        if bwd:
+            dg_.copy_(pin["g"], non_blocking=True)
+            layer.backward(dg_, wgu, wd)
+        for k, v in results:
+            host_out[k].copy_(v, non_blocking=True)
 
     for _ in range(2):
         e2e_step()
@@ -233,7 +248,7 @@ def run_ours(args):
         e2e_ms = float(tt.item())
 
     cpu_base = None
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and bwd:
         cpu_base = oracle_baseline(w, inp, budget_s=args.cpu_seconds)
     if world > 1:
         dist.destroy_process_group()
@@ -242,39 +257,51 @@ def run_ours(args):
 
     peaks = _peaks()
     ms = elapsed_ms / args.steps
-    gemm_ms = per["grouped_ffn_fwd"] + per["grouped_ffn_bwd"]
+    gemm_ms = per["grouped_ffn_fwd"] + (per["grouped_ffn_bwd"] if bwd else 0.0)
     achieved = gemm_flop / (gemm_ms * 1e-3) / 1e12
     peak = peaks["bf16_sustained"] or peaks["bf16"]
-    mem_bytes = {   # algorithmic bytes per call (bf16 rows; indices 4 B)
-        "permute": (w.T * w.d + M * w.d) * 2 + M * 4,
-        "combine_fwd": (M * w.d + w.T * w.d) * 2 + M * 8,
-        "combine_bwd": (w.T * w.d + 2 * M * w.d) * 2 + M * 16 + w.T * w.E * 4,
-        "unpermute": (M * w.d + w.T * w.d) * 2 + M * 4,
+    es = 2 if w.dtype == "bf16" else 4
+    mem_bytes = {   # algorithmic bytes per call (rows in the layer dtype; indices and weights 4 B)
+        "permute": (w.T * w.d + M * w.d) * es + M * 4,
+        "combine_fwd": (M * w.d + w.T * w.d) * es + M * 8,
+        "combine_bwd": (w.T * w.d + 2 * M * w.d) * es + M * 16 + w.T * w.E * 4,
+        "unpermute": (M * w.d + w.T * w.d) * es + M * 4,
     }
-    kern = {n: {"ms": round(v, 4)} for n, v in per.items()}
+    kern = {n: {"ms": round(v, 4)} for n, v in per.items() if bwd or n in names[:5]}
     for n, b in mem_bytes.items():
+        if n not in kern:
+            continue
         kern[n]["GBps"] = round(b / (per[n] * 1e-3) / 1e9, 1)
         kern[n]["frac_hbm"] = round(b / (per[n] * 1e-3) / 1e9 / peaks["hbm"], 3)
     kern["grouped_ffn_fwd"]["TFLOPs"] = round(6.0 * M * w.d * w.f / (per["grouped_ffn_fwd"] * 1e-3) / 1e12, 1)
-    kern["grouped_ffn_bwd"]["TFLOPs"] = round(12.0 * M * w.d * w.f / (per["grouped_ffn_bwd"] * 1e-3) / 1e12, 1)
+    if bwd:
+        kern["grouped_ffn_bwd"]["TFLOPs"] = round(12.0 * M * w.d * w.f / (per["grouped_ffn_bwd"] * 1e-3) / 1e12, 1)
     value = world * w.T * args.steps / (elapsed_ms * 1e-3)
+    if w.dtype == "bf16":
+        roofline = {"kernel": "grouped SwiGLU GEMM (tcgen05; per step: fwd GATEUP, DOWN" +
+                              ("; bwd DH, WGRAD down, DGRAD, WGRAD gate/up)" if bwd else ")"),
+                    "bound": "tensor", "achieved": round(achieved, 1), "peak": peak, "unit": "TFLOP/s",
+                    "frac": round(achieved / peak, 3),
+                    "peak_kind": f"{peaks['src']} bf16 dense, sustained (kernel timed inside a long step)",
+                    "algorithmic_flop_per_step": gemm_flop, "traffic": GEMM_TRAFFIC.get(w.name)}
+    else:   # true-fp32 FFMA path: bound by the FP32 pipes (152 SMs x 128 lanes x 2 FLOP x 2.07 GHz)
+        fp32_peak = 152 * 128 * 2 * 2.07e9 / 1e12
+        roofline = {"kernel": "grouped SwiGLU GEMM (SIMT fp32 FFMA)", "bound": "alu", "achieved": round(achieved, 2),
+                    "peak": round(fp32_peak, 1), "unit": "TFLOP/s", "frac": round(achieved / fp32_peak, 4),
+                    "peak_kind": "nominal FP32 FFMA rate at the maximum SM clock", "algorithmic_flop_per_step": gemm_flop,
+                    "traffic": None}
     line = {
         "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms, 4), "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded; see moe_inputs.py)",
+        "vs_baseline": None, "dtype": w.dtype, "data": "synthetic (seeded; see moe_inputs.py)",
         "config": {"workload": w.name, "T": w.T, "d": w.d, "E": w.E, "k": w.k, "f": w.f, "routing": w.routing,
-                   "pass": "fwd+bwd", "parallelism": f"replicas x{world}",
+                   "pass": "fwd+bwd" if bwd else "fwd", "parallelism": f"replicas x{world}",
                    "l2": "inputs larger than L2 (expert weights 768 MiB, grouped activations > 129 MB); no flush"},
-        "roofline": {"kernel": "grouped SwiGLU GEMM (6 tcgen05 launches per step: fwd GATEUP, DOWN; bwd DH, "
-                               "WGRAD down, DGRAD, WGRAD gate/up)",
-                     "bound": "tensor", "achieved": round(achieved, 1), "peak": peak, "unit": "TFLOP/s",
-                     "frac": round(achieved / peak, 3),
-                     "peak_kind": f"{peaks['src']} bf16 dense, sustained (kernel timed inside a long step)",
-                     "algorithmic_flop_per_step": gemm_flop, "traffic": None},
+        "roofline": roofline,
         "kernels": kern,
         "e2e": {"value": round(world * w.T * args.steps / (e2e_ms * 1e-3), 1), "unit": "tokens/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-        "gpu_launches": layer.launches(True) * args.steps,
+        "gpu_launches": layer.launches(bwd) * args.steps,
         "clocks": clk.summary(),
         "cpu_baseline": cpu_base,
     }
