@@ -133,7 +133,7 @@ def run_ours(args):
     x, logits, wgu, wd = inp["x"], inp["logits"], inp["w_gate_up"], inp["w_down"]
     g = inp.get("g")
     bwd = w.backward
-    layer = MoELayer(w.T, w.d, w.E, w.k, w.f, w.torch_dtype, dev, backward=bwd)
+    layer = MoELayer(w.T, w.d, w.E, w.k, w.f, w.torch_dtype, dev, backward=bwd, recompute=args.recompute)
     stream = torch.cuda.current_stream(dev)
     M = w.T * w.k
     gemm_flop = (18.0 if bwd else 6.0) * M * w.d * w.f
@@ -166,8 +166,9 @@ def run_ours(args):
         L.moe_combine_bwd(g, layer.y_perm, layer.topk_w, layer.topk_idx, layer.row_of_slot, layer.counts,
                           layer.tile_offsets, w.E, layer.dy_perm, layer.d_topk_w, layer.d_logits)
         ev[6].record(stream)
-        L.moe_grouped_ffn_bwd(layer.dy_perm, layer.x_perm, layer.ab, layer.h, wgu, wd, layer.tile_offsets, layer.dab,
-                              layer.dx_perm, layer.dw_gate_up, layer.dw_down, layer.ws_ffn)
+        (L.moe_grouped_ffn_bwd_recompute if args.recompute else L.moe_grouped_ffn_bwd)(
+            layer.dy_perm, layer.x_perm, layer.ab, layer.h, wgu, wd, layer.tile_offsets, layer.dab, layer.dx_perm,
+            layer.dw_gate_up, layer.dw_down, layer.ws_ffn)
         ev[7].record(stream)
         L.moe_combine_fwd(layer.dx_perm, None, layer.row_of_slot, w.T, w.k, layer.dx)
         ev[8].record(stream)
@@ -295,7 +296,8 @@ def run_ours(args):
         "warmup": args.warmup, "ms_per_step": round(ms, 4), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": w.dtype, "data": "synthetic (seeded; see moe_inputs.py)",
         "config": {"workload": w.name, "T": w.T, "d": w.d, "E": w.E, "k": w.k, "f": w.f, "routing": w.routing,
-                   "pass": "fwd+bwd" if bwd else "fwd", "parallelism": f"replicas x{world}",
+                   "pass": ("fwd+bwd (recompute)" if args.recompute else "fwd+bwd") if bwd else "fwd",
+                   "parallelism": f"replicas x{world}",
                    "l2": "inputs larger than L2 (expert weights 768 MiB, grouped activations > 129 MB); no flush"},
         "roofline": roofline,
         "kernels": kern,
@@ -381,6 +383,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--recompute", action="store_true",
+                    help="backward recomputes ab, h from x_perm (selective activation checkpointing)")
     ap.add_argument("--ref-tokens", type=int, default=8)
     args = ap.parse_args()
     if args.warmup < 3:

@@ -171,6 +171,19 @@ int moe_grouped_ffn_bwd(const void *dy_perm, const void *x_perm, const void *ab,
                         void *dw_gate_up, void *dw_down, void *ws, size_t ws_bytes, moe_stream_t stream);
 
 /* ---------------------------------------------------------------------------------------------
+ * Backward with recomputation (brief, section 核心方法: selective activation checkpointing, which
+ * may recompute the SparseMoE module in the backward pass to save memory). Same arguments and
+ * results as moe_grouped_ffn_bwd, but `ab` and `h` are outputs here: they are first recomputed
+ * from x_perm by the forward's GEMM1 (with its SwiGLU epilogue), then the backward runs on them.
+ * The forward may therefore write ab and h into scratch that other layers reuse before this
+ * layer's backward; the cost is one more GEMM1 (4 M d f FLOP).
+ */
+int moe_grouped_ffn_bwd_recompute(const void *dy_perm, const void *x_perm, void *ab, void *h, const void *w_gate_up,
+                                  const void *w_down, const int32_t *tile_offsets, int E, int d, int f,
+                                  int64_t rows_max, int dtype, void *dab, void *dx_perm, void *dw_gate_up,
+                                  void *dw_down, void *ws, size_t ws_bytes, moe_stream_t stream);
+
+/* ---------------------------------------------------------------------------------------------
  * Weighted un-permute (combine) back to token order:
  *   out[t] = sum_j topk_w[t,j] * y_perm[row_of_slot[t*k+j]]   (fp32 accumulation in slot order)
  * With topk_w == NULL the rows are summed unweighted: the backward of moe_permute

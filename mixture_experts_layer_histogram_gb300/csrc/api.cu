@@ -71,6 +71,33 @@ extern "C" int moe_grouped_ffn_bwd(const void *dy_perm, const void *x_perm, cons
                             dw_gate_up, dw_down, static_cast<WsHeader *>(ws), s);
 }
 
+extern "C" int moe_grouped_ffn_bwd_recompute(const void *dy_perm, const void *x_perm, void *ab, void *h,
+                                             const void *w_gate_up, const void *w_down, const int32_t *tile_offsets,
+                                             int E, int d, int f, int64_t rows_max, int dtype, void *dab,
+                                             void *dx_perm, void *dw_gate_up, void *dw_down, void *ws,
+                                             size_t ws_bytes, moe_stream_t stream) {
+  int rc = check_ffn_shape(E, d, f, rows_max, dtype, ws, ws_bytes);
+  if (rc) return rc;
+  const void *ptrs[] = {dy_perm, x_perm, ab, h, w_gate_up, w_down, dab, dx_perm, dw_gate_up, dw_down};
+  if (rows_max > 0)
+    for (const void *q : ptrs)
+      if (!q || !aligned16(q)) return MOE_ERR_INVALID_ARG;
+  if (!tile_offsets) return MOE_ERR_INVALID_ARG;
+  if (rows_max == 0) return MOE_OK;
+  cudaStream_t s = (cudaStream_t)stream;
+  // 1. a, b and h again from x_perm (the forward's GEMM1 with its SwiGLU epilogue)
+  if (dtype == MOE_F32)
+    rc = simt_grouped_ffn_fwd((const float *)x_perm, (const float *)w_gate_up, (const float *)w_down, tile_offsets, E,
+                              d, f, rows_max, (float *)ab, (float *)h, nullptr, s);
+  else
+    rc = tc_grouped_ffn_fwd(x_perm, w_gate_up, w_down, tile_offsets, E, d, f, rows_max, ab, h, nullptr,
+                            static_cast<WsHeader *>(ws), s);
+  if (rc) return rc;
+  // 2. the backward on the recomputed activations
+  return moe_grouped_ffn_bwd(dy_perm, x_perm, ab, h, w_gate_up, w_down, tile_offsets, E, d, f, rows_max, dtype, dab,
+                             dx_perm, dw_gate_up, dw_down, ws, ws_bytes, stream);
+}
+
 extern "C" int moe_read_status(const void *ws, moe_stream_t stream) {
   if (!ws) return MOE_ERR_INVALID_ARG;
   int32_t st = 0;

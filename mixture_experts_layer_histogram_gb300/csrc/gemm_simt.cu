@@ -131,7 +131,7 @@ int simt_grouped_ffn_fwd(const float *x, const float *wgu, const float *wd, cons
   a.N = f; a.K = d;
   a.C = ab; a.ldc = 2 * (int64_t)f; a.C2 = h; a.ldc2 = f;
   int rc = launch<GATEUP>(a, rows_max, f, 1, s);
-  if (rc) return rc;
+  if (rc || y == nullptr) return rc;   // y == nullptr: GEMM1 only (recompute of ab, h)
   // y = h Wd^T
   a.A = h; a.sAm = f; a.sAk = 1;
   a.B = wd; a.sBn = f; a.sBk = 1; a.sBe = (int64_t)d * f; a.up_off = 0;

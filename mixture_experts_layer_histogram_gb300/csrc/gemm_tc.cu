@@ -926,7 +926,7 @@ int tc_grouped_ffn_fwd(const void *x_perm, const void *wgu, const void *wd, cons
   p.ld1 = f;
   int rc = launch<GATEUP>(mA, mB, mC0, mC1, p, row_tiles * p.n_tiles, pair_rows * p.n_tiles,
                           use_pair(GATEUP, rows_max, E), s);
-  if (rc) return rc;
+  if (rc || y == nullptr) return rc;   // y == nullptr: GEMM1 only (recompute of ab, h)
   // GEMM2: y = h Wd^T
   if (!make_map(&mA, h, rows_max, f, 128) || !make_map(&mB, wd, (uint64_t)E * d, f, 128) ||
       !make_store_map(&mC0, y, rows_max, d))

@@ -24,7 +24,11 @@ from . import _lib as L
 class MoELayer:
     """Buffers of one layer pass, allocated once and reused every step (no allocation per step)."""
 
-    def __init__(self, T, d, E, k, f, dtype=torch.bfloat16, device="cuda", backward=True):
+    def __init__(self, T, d, E, k, f, dtype=torch.bfloat16, device="cuda", backward=True, recompute=False,
+                 scratch=None):
+        """recompute: the backward recomputes ab and h from x_perm instead of reading them (selective
+        activation checkpointing); ab and h may then live in `scratch` (a dict with tensors "ab" [R, 2f]
+        and "h" [R, f] shared with other layers)."""
         if not torch.cuda.is_available():
             raise RuntimeError("MoELayer needs a CUDA device")
         self.T, self.d, self.E, self.k, self.f = T, d, E, k, f
@@ -45,8 +49,12 @@ class MoELayer:
         self.ws_ffn = torch.zeros(L.moe_grouped_ffn_workspace_size(E, d, f, R, L.dtype_code(dtype), backward),
                                   dtype=torch.uint8, device=self.device)
         self.x_perm = torch.empty((R, d), **act)
-        self.ab = torch.empty((R, 2 * f), **act)
-        self.h = torch.empty((R, f), **act)
+        self.recompute = recompute
+        if scratch is not None:
+            self.ab, self.h = scratch["ab"], scratch["h"]
+        else:
+            self.ab = torch.empty((R, 2 * f), **act)
+            self.h = torch.empty((R, f), **act)
         self.y_perm = torch.empty((R, d), **act)
         self.out = torch.empty((T, d), **act)
         self.backward_enabled = backward
@@ -75,8 +83,9 @@ class MoELayer:
             raise RuntimeError("layer was built without backward buffers")
         L.moe_combine_bwd(grad_out, self.y_perm, self.topk_w, self.topk_idx, self.row_of_slot, self.counts,
                           self.tile_offsets, self.E, self.dy_perm, self.d_topk_w, self.d_logits, stream)
-        L.moe_grouped_ffn_bwd(self.dy_perm, self.x_perm, self.ab, self.h, w_gate_up, w_down, self.tile_offsets,
-                              self.dab, self.dx_perm, self.dw_gate_up, self.dw_down, self.ws_ffn, stream)
+        bwd = L.moe_grouped_ffn_bwd_recompute if self.recompute else L.moe_grouped_ffn_bwd
+        bwd(self.dy_perm, self.x_perm, self.ab, self.h, w_gate_up, w_down, self.tile_offsets, self.dab, self.dx_perm,
+            self.dw_gate_up, self.dw_down, self.ws_ffn, stream)
         L.moe_combine_fwd(self.dx_perm, None, self.row_of_slot, self.T, self.k, self.dx, stream)
         return dict(dx=self.dx, d_logits=self.d_logits, d_topk_w=self.d_topk_w, dw_gate_up=self.dw_gate_up,
                     dw_down=self.dw_down)
@@ -88,4 +97,4 @@ class MoELayer:
     # kernels launched per pass, for the bench's launch count
     def launches(self, backward=True):
         fwd = 1 + 2 + 1 + 2 + 1
-        return fwd + (1 + 4 + 1 if backward else 0)
+        return fwd + ((1 + 4 + 1 + (1 if self.recompute else 0)) if backward else 0)
