@@ -4,5 +4,6 @@ and the weighted combine, forward and backward, behind the C ABI in include/moe.
 from . import _lib
 from ._lib import MoeError
 from .layer import MoELayer
+from .pipeline import HostPipeline
 
-__all__ = ["MoELayer", "MoeError", "_lib"]
+__all__ = ["MoELayer", "HostPipeline", "MoeError", "_lib"]
