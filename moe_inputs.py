@@ -122,6 +122,12 @@ def make_logits(w: Workload, device="cpu", x=None):
     raise ValueError(w.routing)
 
 
+def make_router_weight(w: Workload, device="cpu"):
+    """Router weight W_r [E, d] (row e scores expert e), ~ N(0, 0.02): the same draw that the
+    "router" logits recipe multiplies by, stored transposed (L = x W_r^T)."""
+    return _normal((w.d, w.E), 0.02, w.torch_dtype, device, w.seed, "router").t().contiguous()
+
+
 def make_x(w: Workload, device="cpu"):
     return _normal((w.T, w.d), 1.0, w.torch_dtype, device, w.seed, "x")
 

@@ -15,6 +15,8 @@ the definition it computes in the C source; the short form:
                   dw, d_logits (softmax backward on S_t), dx_t
   moe_dweights    dW_gate_up, dW_down summed over all tokens
   dweight_entries selected dW entries, each summed over the tokens routed to its expert
+  router_logits   L[t,e] = sum_c x[t,c] Wr[e,c]   (the router before the selection)
+  router_dx       dx_r[t,c] = sum_e dL[t,e] Wr[e,c];  router_dw  dWr[e,c] = sum_t dL[t,e] x[t,c]
 
 Parity pins (tests/test_oracle_*.py): brute-force index/top-k on tiny inputs, invariants, the E=1/k=1
 reduction to a plain SwiGLU FFN, dense routing k=E, W_down=0, equal logits, forced-uniform counts,
@@ -62,8 +64,11 @@ def lib():
             L.oracle_moe_tokens.argtypes = [I, I, I, I, I, P, I, P, P, P, P, I, P, I, P, I64, P, P, P, P, P]
             L.oracle_moe_dweights.argtypes = [I, I, I, I, I, P, I, P, P, P, P, I, P, I, P, P]
             L.oracle_moe_dweight_entries.argtypes = [I, I, I, I, I, P, I, P, P, P, P, I, P, I, I64, P, P, P, P, P]
+            L.oracle_router_logits.argtypes = [I, I, I, P, I, P, I, P, I64, P]
+            L.oracle_router_dx.argtypes = [I, I, I, P, I, P, I, P, I64, P]
+            L.oracle_router_dw.argtypes = [I, I, I, P, I, P, I, P, I64, P]
             for fn in ("oracle_route_topk", "oracle_index", "oracle_moe_tokens", "oracle_moe_dweights",
-                       "oracle_moe_dweight_entries"):
+                       "oracle_moe_dweight_entries", "oracle_router_logits", "oracle_router_dx", "oracle_router_dw"):
                 getattr(L, fn).restype = I
             _lib = L
     return _lib
@@ -192,3 +197,50 @@ def dweight_entries(x, idx, w, w_gate_up, w_down, g, mat, e, r, c):
                                             wdt, _ptr(G), gdt, n, *[_ptr(v) for v in cols], _ptr(val)),
            "dweight_entries")
     return val
+
+
+def _tokens(tokens, T):
+    if tokens is None:
+        return None, T
+    tok = torch.as_tensor(tokens, dtype=torch.int64).contiguous()
+    return tok, tok.numel()
+
+
+def router_logits(x, w_router, tokens=None):
+    """L = x Wr^T for the listed tokens (all if None); Wr is [E, d]. fp64 [n, E]."""
+    X, xdt = _cpu(x)
+    Wr, wdt = _cpu(w_router)
+    T, d = X.shape
+    E = Wr.shape[0]
+    tok, n = _tokens(tokens, T)
+    out = torch.empty((n, E), dtype=torch.float64)
+    _check(lib().oracle_router_logits(T, d, E, _ptr(X), xdt, _ptr(Wr), wdt, _ptr(tok), n, _ptr(out)), "router_logits")
+    return out
+
+
+def router_dx(d_logits, w_router, tokens=None):
+    """dx_r = dL Wr for the listed tokens (all if None). fp64 [n, d]."""
+    DL, dldt = _cpu(d_logits)
+    Wr, wdt = _cpu(w_router)
+    T, E = DL.shape
+    d = Wr.shape[1]
+    tok, n = _tokens(tokens, T)
+    out = torch.empty((n, d), dtype=torch.float64)
+    _check(lib().oracle_router_dx(T, d, E, _ptr(DL), dldt, _ptr(Wr), wdt, _ptr(tok), n, _ptr(out)), "router_dx")
+    return out
+
+
+def router_dw(x, d_logits, cols=None):
+    """dWr = dL^T x for the listed columns of Wr (all if None). fp64 [E, ncols]."""
+    X, xdt = _cpu(x)
+    DL, dldt = _cpu(d_logits)
+    T, d = X.shape
+    E = DL.shape[1]
+    if cols is None:
+        cl, nc = None, d
+    else:
+        cl = torch.as_tensor(cols, dtype=torch.int32).contiguous()
+        nc = cl.numel()
+    out = torch.empty((E, nc), dtype=torch.float64)
+    _check(lib().oracle_router_dw(T, d, E, _ptr(X), xdt, _ptr(DL), dldt, _ptr(cl), nc, _ptr(out)), "router_dw")
+    return out

@@ -311,3 +311,62 @@ int oracle_moe_dweight_entries(int T, int d, int E, int k, int f, const void *x,
   }
   return bad ? -2 : 0;
 }
+
+/*
+ * The router, the step before the selection ("Scalable Pretraining of Large MoE LMs on Aurora",
+ * summary page, section 关键设计: expert selection): a linear map from the token to one logit per
+ * expert, L[t,e] = sum_c x[t,c] Wr[e,c], with Wr stored [E, d]. Its backward for a given dL is
+ *   dx_r[t,c] = sum_e dL[t,e] Wr[e,c]      (added to the experts' dx_t by the layer)
+ *   dWr[e,c]  = sum_t dL[t,e] x[t,c].
+ * tok (n entries, NULL = all T tokens) lists the rows to evaluate; cols (NULL = all d) the columns
+ * of dWr. Results are fp64, rows in list order.
+ */
+int oracle_router_logits(int T, int d, int E, const void *x, int x_dt, const void *wr, int w_dt, const int64_t *tok,
+                         int64_t n, double *L) {
+  if (T < 0 || d <= 0 || E <= 0) return -1;
+  int bad = 0;
+#pragma omp parallel for schedule(static)
+  for (int64_t i = 0; i < n; ++i) {
+    int64_t t = tok ? tok[i] : i;
+    if (t < 0 || t >= T) { bad = 1; continue; }
+    for (int e = 0; e < E; ++e) {
+      double s = 0.0;
+      for (int c = 0; c < d; ++c) s += ld(x, (size_t)t * d + c, x_dt) * ld(wr, (size_t)e * d + c, w_dt);
+      L[(size_t)i * E + e] = s;
+    }
+  }
+  return bad ? -2 : 0;
+}
+
+int oracle_router_dx(int T, int d, int E, const void *dl, int dl_dt, const void *wr, int w_dt, const int64_t *tok,
+                     int64_t n, double *dx) {
+  if (T < 0 || d <= 0 || E <= 0) return -1;
+  int bad = 0;
+#pragma omp parallel for schedule(static)
+  for (int64_t i = 0; i < n; ++i) {
+    int64_t t = tok ? tok[i] : i;
+    if (t < 0 || t >= T) { bad = 1; continue; }
+    for (int c = 0; c < d; ++c) {
+      double s = 0.0;
+      for (int e = 0; e < E; ++e) s += ld(dl, (size_t)t * E + e, dl_dt) * ld(wr, (size_t)e * d + c, w_dt);
+      dx[(size_t)i * d + c] = s;
+    }
+  }
+  return bad ? -2 : 0;
+}
+
+int oracle_router_dw(int T, int d, int E, const void *x, int x_dt, const void *dl, int dl_dt, const int32_t *cols,
+                     int64_t ncols, double *dw) {
+  if (T < 0 || d <= 0 || E <= 0) return -1;
+  int bad = 0;
+#pragma omp parallel for schedule(dynamic, 1)
+  for (int e = 0; e < E; ++e)
+    for (int64_t j = 0; j < ncols; ++j) {
+      int c = cols ? cols[j] : (int)j;
+      if (c < 0 || c >= d) { bad = 1; continue; }
+      double s = 0.0;
+      for (int t = 0; t < T; ++t) s += ld(dl, (size_t)t * E + e, dl_dt) * ld(x, (size_t)t * d + c, x_dt);
+      dw[(size_t)e * ncols + j] = s;
+    }
+  return bad ? -2 : 0;
+}
