@@ -205,8 +205,47 @@ int moe_combine_bwd(const void *grad_out, const void *y_perm, const float *topk_
                     float *d_logits, moe_stream_t stream);
 
 /* ---------------------------------------------------------------------------------------------
+ * Router, the step before the selection (summary page, section 关键设计: expert selection). The
+ * logits are a linear map of the token, L[t,e] = sum_c x[t,c] w_router[e,c] (fp32 accumulation),
+ * followed in the same kernel by the selection and weights of moe_route_topk:
+ *   x          [T, d]  dtype
+ *   w_router   [E, d]  dtype; row e scores expert e
+ *   logits     [T, E]  fp32 output, or NULL when the caller does not need the logits
+ *   topk_idx   [T, k]  int32: the k largest logits, ordered by (logit desc, id asc), -0 == +0
+ *   topk_w     [T, k]  fp32: softmax over the selected logits. The selection is the one
+ *                      moe_route_topk makes on the same fp32 logits; the weights may differ from
+ *                      moe_route_topk's in the last bit (here the selected exponentials are summed
+ *                      in slot order).
+ * bf16: one tcgen05 kernel (TMA-fed tiles of 128 tokens x all E experts, the fp32 accumulator in
+ * TMEM, the top-k and softmax in the epilogue, one thread per token); requires d % 8 == 0.
+ * fp32: SIMT fp32 FMA, then the moe_route_topk kernel on the logits; any d >= 1.
+ * Requires 1 <= E <= MOE_MAX_EXPERTS, 1 <= k <= min(E, MOE_MAX_TOPK), T >= 0, and
+ * ws: moe_router_workspace_size(T, d, E, dtype) bytes of device memory, 256-byte aligned, any
+ * content (device status word; scratch of the fp32 path and of the backward). Device errors:
+ * MOE_ERR_DEVICE_TIMEOUT (every pipeline wait of the bf16 kernels is bounded to about 0.2 s).
+ */
+size_t moe_router_workspace_size(int T, int d, int E, int dtype);
+int moe_router_fwd(const void *x, const void *w_router, int T, int d, int E, int k, int dtype, float *logits,
+                   int32_t *topk_idx, float *topk_w, void *ws, size_t ws_bytes, moe_stream_t stream);
+
+/*
+ * Router backward, for d_logits [T, E] fp32 (from moe_combine_bwd):
+ *   dx         [T, d]  dtype   accumulate_dx = 0:  dx  = d_logits w_router
+ *                              accumulate_dx = 1:  dx += d_logits w_router  (adds the router's
+ *                              share to the experts' dx; read and written in place)
+ *   dw_router  [E, d]  dtype   d_logits^T x  (overwritten, not accumulated)
+ * bf16: d_logits is rounded to bf16 once (the tensor-core operand); both products run on tcgen05
+ * with fp32 accumulation; dw_router is the sum, in a fixed order, of fp32 partial products over
+ * token ranges (deterministic). fp32: SIMT fp32 FMA. Same shape rules and workspace as the
+ * forward (the same ws may serve both calls when they are ordered on one stream).
+ */
+int moe_router_bwd(const void *x, const void *w_router, const float *d_logits, int T, int d, int E, int dtype,
+                   int accumulate_dx, void *dx, void *dw_router, void *ws, size_t ws_bytes, moe_stream_t stream);
+
+/* ---------------------------------------------------------------------------------------------
  * Synchronises `stream`, then returns the device status word at the start of a workspace used by
- * moe_count_index or moe_grouped_ffn_*: MOE_OK or a negative moe_status. Not for the hot path.
+ * moe_count_index, moe_grouped_ffn_* or moe_router_*: MOE_OK or a negative moe_status. Not for
+ * the hot path.
  */
 int moe_read_status(const void *ws, moe_stream_t stream);
 const char *moe_status_string(int status);

@@ -40,6 +40,9 @@ _SIGS = {
                                            _P]),
     "moe_combine_fwd": (_I, [_P, _P, _P, _I, _I, _I, _I64, _I, _P, _P]),
     "moe_combine_bwd": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I64, _I, _P, _P, _P, _P]),
+    "moe_router_workspace_size": (_SZ, [_I, _I, _I, _I]),
+    "moe_router_fwd": (_I, [_P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P, _SZ, _P]),
+    "moe_router_bwd": (_I, [_P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _SZ, _P]),
     "moe_read_status": (_I, [_P, _P]),
     "moe_status_string": (ctypes.c_char_p, [_I]),
     "moe_version": (_I, []),
@@ -178,6 +181,27 @@ def moe_combine_bwd(grad_out, y_perm, topk_w, topk_idx, row_of_slot, counts, til
     _ok("moe_combine_bwd", lib().moe_combine_bwd(
         _p(grad_out), _p(y_perm), _p(topk_w), _p(topk_idx), _p(row_of_slot), _p(counts), _p(tile_offsets), T, d, k, E,
         y_perm.shape[0], dtype_code(y_perm.dtype), _p(dy_perm), _p(d_topk_w), _p(d_logits), _s(stream)))
+
+
+def moe_router_workspace_size(T, d, E, dtype):
+    return int(lib().moe_router_workspace_size(T, d, E, dtype))
+
+
+def moe_router_fwd(x, w_router, k, logits, topk_idx, topk_w, ws, stream=None):
+    """logits may be None (not written)."""
+    T, d = x.shape
+    E = w_router.shape[0]
+    _ok("moe_router_fwd", lib().moe_router_fwd(
+        _p(x), _p(w_router), T, d, E, k, dtype_code(x.dtype), _p(logits), _p(topk_idx), _p(topk_w), _p(ws),
+        ws.numel() * ws.element_size(), _s(stream)))
+
+
+def moe_router_bwd(x, w_router, d_logits, dx, dw_router, ws, accumulate_dx=False, stream=None):
+    T, d = x.shape
+    E = w_router.shape[0]
+    _ok("moe_router_bwd", lib().moe_router_bwd(
+        _p(x), _p(w_router), _p(d_logits), T, d, E, dtype_code(x.dtype), int(bool(accumulate_dx)), _p(dx),
+        _p(dw_router), _p(ws), ws.numel() * ws.element_size(), _s(stream)))
 
 
 def moe_read_status(ws, stream=None):

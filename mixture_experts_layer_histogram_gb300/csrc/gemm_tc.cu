@@ -20,12 +20,17 @@
 //   DH      dh = dy Wd[e]  (B read MN-major), epilogue reads a, b and writes da, db
 //   DGRAD   dx = dab Wgu[e] (B read MN-major)
 //   WGRAD   dW[e] = act1_e^T act2_e over expert e's rows (A and B read MN-major, K = rows of e)
+// and two kinds of the router's backward (single-CTA kernel only; one "group" = all tokens for
+// RDX, one token range per group for RDW):
+//   RDX     dx (+)= dL Wr   (B read MN-major; the epilogue adds the previous dx when asked)
+//   RDW     fp32 partial dWr = dL_g^T x_g over token range g (A and B MN-major), plain fp32 stores
 // Every wait is bounded (0.2 s); on timeout the kernel records MOE_ERR_DEVICE_TIMEOUT in the
 // workspace status word, lets in-flight copies and MMAs land, frees TMEM and returns.
 #include <cuda.h>
 
 #include "common.cuh"
 #include "tc_ptx.cuh"
+#include "tma_host.cuh"
 
 namespace moe {
 namespace tc {
@@ -41,7 +46,9 @@ constexpr int TMEM_COLS = 2 * BN;           // two fp32 accumulators of 128 lane
 constexpr int MAX_E = MOE_MAX_EXPERTS;
 constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 32 * 32 * 2 * 2 * EPI_WARPS + 1024 + 256;
 
-enum Kind { GATEUP = 0, DOWN = 1, DH = 2, DGRAD = 3, WGRAD = 4 };
+enum Kind { GATEUP = 0, DOWN = 1, DH = 2, DGRAD = 3, WGRAD = 4, RDX = 5, RDW = 6 };
+// kinds whose tiles reduce over the rows of one group (A and B read MN-major)
+__host__ __device__ constexpr bool row_reduce(int kind) { return kind == WGRAD || kind == RDW; }
 
 struct Params {
   const int32_t *tile_offsets;
@@ -58,6 +65,9 @@ struct Params {
   const __nv_bfloat16 *aux;
   int64_t ld_aux;
   int64_t out_e_stride;
+  float *outf;        // RDW: fp32 partials [groups, rows_valid, ldf]
+  int64_t ldf;
+  int rows_valid;     // RDX: rows of dx (tokens); RDW: rows of dWr (experts)
 };
 
 // Instruction descriptor, kind::f16: D fp32, A and B bf16, M = 128, N = 256, K-major unless *_mn.
@@ -78,7 +88,7 @@ struct Tile {
 template <int KIND>
 __device__ __forceinline__ Tile decode(int tile, const Params &p, const int *toff) {
   Tile t;
-  if (KIND == WGRAD) {
+  if (row_reduce(KIND)) {
     const int per = p.m_tiles * p.n_tiles;
     t.e = tile / per;
     const int r = tile - t.e * per;
@@ -211,13 +221,47 @@ __device__ __forceinline__ void epilogue_tile(const Tile &t, const Params &p, ui
 #pragma unroll
       for (int i = 0; i < 8; ++i) cur[i] = nxt[i];
     }
-  } else {
+  } else if (KIND == RDW) {
+    // fp32 partial of token range t.e; rows are experts, stored for the first rows_valid only
+    const int er = t.m0 + row;
+    float *dst = p.outf + ((int64_t)t.e * p.rows_valid + er) * p.ldf + t.n0;
 #pragma unroll 1
     for (int c = c0; c < c0 + BN / 2; c += 32) {
       tmem_ld32(tbase + c, r);
       tmem_ld_wait();
+      if (er < p.rows_valid) {
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+          if (t.n0 + c + 4 * q < p.d)
+            *reinterpret_cast<float4 *>(dst + c + 4 * q) =
+                make_float4(__uint_as_float(r[4 * q]), __uint_as_float(r[4 * q + 1]), __uint_as_float(r[4 * q + 2]),
+                            __uint_as_float(r[4 * q + 3]));
+      }
+    }
+  } else {
+    // RDX with an addend: this row's previous dx (rows past the tokens and columns past d are not
+    // read; the store map drops them)
+    const bool add = KIND == RDX && p.aux != nullptr && t.m0 + row < p.rows_valid;
+    const __nv_bfloat16 *arow = add ? p.aux + (int64_t)(t.m0 + row) * p.ld_aux + t.n0 : nullptr;
+#pragma unroll 1
+    for (int c = c0; c < c0 + BN / 2; c += 32) {
+      uint4 q[4] = {};
+      if (KIND == RDX && add) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+          if (t.n0 + c + 8 * i < p.d) q[i] = *reinterpret_cast<const uint4 *>(arow + c + 8 * i);
+      }
+      tmem_ld32(tbase + c, r);
+      tmem_ld_wait();
 #pragma unroll
       for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+      if (KIND == RDX && add) {
+        float av[32];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) unpack_bf16x8(q[i], av + 8 * i);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) v[i] += av[i];
+      }
       es.put(mc0, t.n0 + c, yrow, v);
     }
   }
@@ -234,8 +278,8 @@ template <int KIND>
 __global__ void __launch_bounds__(THREADS, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmC0, const __grid_constant__ CUtensorMap tmC1, const Params p) {
-  constexpr bool A_MN = (KIND == WGRAD);
-  constexpr bool B_MN = (KIND == DH || KIND == DGRAD || KIND == WGRAD);
+  constexpr bool A_MN = row_reduce(KIND);
+  constexpr bool B_MN = (KIND == DH || KIND == DGRAD || KIND == RDX || row_reduce(KIND));
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t *epi_smem = smem + STAGES * STAGE_BYTES;
@@ -280,7 +324,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   tc_fence_after();
   const uint32_t tmem_base = *tmem_holder;
 
-  const int num_tiles = (KIND == WGRAD) ? p.E * p.m_tiles * p.n_tiles : toff[p.E] * p.n_tiles;
+  const int num_tiles = row_reduce(KIND) ? p.E * p.m_tiles * p.n_tiles : toff[p.E] * p.n_tiles;
 
   if (warp == 0 && lane == 0) {
     // ------------------------------------------------------------------ TMA producer
@@ -304,11 +348,11 @@ __global__ void __launch_bounds__(THREADS, 1)
           tma_load_2d(sA, &tmA, kx, t.m0, fb);
           tma_load_2d(sB, &tmB, kx, t.e * p.b_rows_e + t.n0, fb);
           tma_load_2d(sB + B_BYTES / 2, &tmB, kx, t.e * p.b_rows_e + t.n0 + BN / 2, fb);
-        } else if (KIND == DH || KIND == DGRAD) {
+        } else if (KIND == DH || KIND == DGRAD || KIND == RDX) {
           tma_load_2d(sA, &tmA, kx, t.m0, fb);
 #pragma unroll
           for (int q = 0; q < BN / 64; ++q) tma_load_2d(sB + q * 8192, &tmB, t.n0 + 64 * q, t.e * p.b_rows_e + kx, fb);
-        } else {   // WGRAD
+        } else {   // WGRAD, RDW
 #pragma unroll
           for (int q = 0; q < BM / 64; ++q) tma_load_2d(sA + q * 8192, &tmA, t.m0 + 64 * q, t.krow0 + kx, fb);
 #pragma unroll
@@ -375,11 +419,20 @@ __global__ void __launch_bounds__(THREADS, 1)
     uint32_t acc_phase = 0;
     for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
       const Tile t = decode<KIND>(tile, p, toff);
-      if (t.kb == 0) {   // WGRAD of an expert with no rows: the gradient is zero
-        __nv_bfloat16 *dst =
-            p.out0 + (int64_t)t.e * p.out_e_stride + (int64_t)(t.m0 + row_in_tile) * p.ld0 + t.n0 + c0;
-        uint4 *q = reinterpret_cast<uint4 *>(dst);
-        for (int i = 0; i < BN / 16; ++i) q[i] = make_uint4(0, 0, 0, 0);
+      if (t.kb == 0) {   // a group with no rows: its gradient (partial) is zero
+        if (KIND == RDW) {
+          const int er = t.m0 + row_in_tile;
+          if (er < p.rows_valid) {
+            float *dst = p.outf + ((int64_t)t.e * p.rows_valid + er) * p.ldf + t.n0 + c0;
+            for (int i = 0; i < BN / 2; i += 4)
+              if (t.n0 + c0 + i < p.d) *reinterpret_cast<float4 *>(dst + i) = make_float4(0.f, 0.f, 0.f, 0.f);
+          }
+        } else {
+          __nv_bfloat16 *dst =
+              p.out0 + (int64_t)t.e * p.out_e_stride + (int64_t)(t.m0 + row_in_tile) * p.ld0 + t.n0 + c0;
+          uint4 *q = reinterpret_cast<uint4 *>(dst);
+          for (int i = 0; i < BN / 16; ++i) q[i] = make_uint4(0, 0, 0, 0);
+        }
         continue;
       }
       uint4 pre[8];
@@ -763,11 +816,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     for (int tile = cluster_id; tile < num_tiles; tile += num_clusters) {
       bool valid;
       const Tile t = decode_pair<KIND>(tile, p, toff, ptoff, (int)rank, valid);
-      if (t.kb == 0) {   // WGRAD of an expert with no rows: the gradient is zero
-        __nv_bfloat16 *dst =
-            p.out0 + (int64_t)t.e * p.out_e_stride + (int64_t)(t.m0 + row_in_tile) * p.ld0 + t.n0 + c0;
-        uint4 *q = reinterpret_cast<uint4 *>(dst);
-        for (int i = 0; i < BN / 16; ++i) q[i] = make_uint4(0, 0, 0, 0);
+      if (t.kb == 0) {   // a group with no rows: its gradient (partial) is zero
+        if (KIND == RDW) {
+          const int er = t.m0 + row_in_tile;
+          if (er < p.rows_valid) {
+            float *dst = p.outf + ((int64_t)t.e * p.rows_valid + er) * p.ldf + t.n0 + c0;
+            for (int i = 0; i < BN / 2; i += 4)
+              if (t.n0 + c0 + i < p.d) *reinterpret_cast<float4 *>(dst + i) = make_float4(0.f, 0.f, 0.f, 0.f);
+          }
+        } else {
+          __nv_bfloat16 *dst =
+              p.out0 + (int64_t)t.e * p.out_e_stride + (int64_t)(t.m0 + row_in_tile) * p.ld0 + t.n0 + c0;
+          uint4 *q = reinterpret_cast<uint4 *>(dst);
+          for (int i = 0; i < BN / 16; ++i) q[i] = make_uint4(0, 0, 0, 0);
+        }
         continue;
       }
       uint4 pre[8];
@@ -816,45 +878,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
 }
 
 // ----------------------------------------------------------------------------- host side -------
-typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
-                                  const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
-                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-static EncodeTiledFn encode_fn() {
-  static EncodeTiledFn fn = nullptr;
-  if (!fn) {
-    void *ptr = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
-            cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<EncodeTiledFn>(ptr);
-  }
-  return fn;
-}
-
-// 2D bf16 row-major [rows, cols] with box = box_cols x box_rows and the given swizzle.
-static bool encode_map(CUtensorMap *m, const void *base, uint64_t rows, uint64_t cols, uint32_t box_cols,
-                       uint32_t box_rows, CUtensorMapSwizzle swz) {
-  EncodeTiledFn enc = encode_fn();
-  if (!enc) return false;
-  cuuint64_t dims[2] = {cols, rows};
-  cuuint64_t strides[1] = {cols * 2};
-  cuuint32_t box[2] = {box_cols, box_rows};
-  cuuint32_t estr[2] = {1, 1};
-  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box, estr,
-             CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-// operand loads: 64 columns (128 B, the swizzle span) x box_rows rows, 128-byte swizzle
-static bool make_map(CUtensorMap *m, const void *base, uint64_t rows, uint64_t cols, uint32_t box_rows) {
-  return encode_map(m, base, rows, cols, 64, box_rows, CU_TENSOR_MAP_SWIZZLE_128B);
-}
-// epilogue stores: 32 x 32 blocks, 64-byte swizzle (matches EpiStore's shared-memory layout)
-static bool make_store_map(CUtensorMap *m, const void *base, uint64_t rows, uint64_t cols) {
-  return encode_map(m, base, rows, cols, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B);
-}
-
 constexpr uint32_t MN_BOX = P_BK;   // k rows of an MN-major TMA box (both kernels take P_BK == BK)
 static_assert(P_BK == BK, "the single-CTA and pair kernels share the MN-major tensor maps");
 
@@ -863,6 +886,19 @@ static_assert(P_BK == BK, "the single-CTA and pair kernels share the MN-major te
 static bool use_pair(int kind, int64_t rows_max, int E) {
   if (kind == WGRAD) return true;   // pairs along the weight rows: no waste
   return rows_max / BM >= 4 * (int64_t)E;
+}
+
+// The single-CTA kernel on a persistent grid of min(SMs, max_tiles) CTAs.
+template <int KIND>
+static int launch_single(const CUtensorMap &a, const CUtensorMap &b, const CUtensorMap &c0, const CUtensorMap &c1,
+                         const Params &p, int64_t max_tiles, cudaStream_t s) {
+  MOE_TRY_CUDA(cudaFuncSetAttribute(tc_gemm_kernel<KIND>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES));
+  int64_t grid = sm_count();
+  if (max_tiles < grid) grid = max_tiles;
+  if (grid < 1) grid = 1;
+  tc_gemm_kernel<KIND><<<(int)grid, THREADS, SMEM_BYTES, s>>>(a, b, c0, c1, p);
+  MOE_CHECK_LAUNCH();
+  return MOE_OK;
 }
 
 // max_tiles / max_pair_tiles: host upper bounds on the tile counts (the exact counts live on the device)
@@ -889,13 +925,7 @@ static int launch(const CUtensorMap &a, const CUtensorMap &b, const CUtensorMap 
     MOE_CHECK_LAUNCH();
     return MOE_OK;
   }
-  MOE_TRY_CUDA(cudaFuncSetAttribute(tc_gemm_kernel<KIND>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES));
-  int64_t grid = sm_count();
-  if (max_tiles < grid) grid = max_tiles;
-  if (grid < 1) grid = 1;
-  tc_gemm_kernel<KIND><<<(int)grid, THREADS, SMEM_BYTES, s>>>(a, b, c0, c1, p);
-  MOE_CHECK_LAUNCH();
-  return MOE_OK;
+  return launch_single<KIND>(a, b, c0, c1, p, max_tiles, s);
 }
 
 }  // namespace tc
@@ -1005,6 +1035,50 @@ int tc_grouped_ffn_bwd(const void *dy, const void *x_perm, const void *ab, const
   p.out_e_stride = (int64_t)2 * f * d;
   return launch<WGRAD>(mA, mB, mC, mC, p, (int64_t)E * p.m_tiles * p.n_tiles, (int64_t)E * (p.m_tiles / 2) * p.n_tiles,
                        use_pair(WGRAD, rows_max, E), s);
+}
+
+// Router backward GEMMs (router.cu prepares dl16, the bf16 copy of d_logits [t_pad, ek] with zero
+// padding, and the group offsets in 128-row tiles).
+// dx (+)= dL Wr: one group of t_pad / 128 row tiles; B = Wr [E, d] read MN-major (rows >= E read as 0).
+int tc_router_dx(const void *dl16, int64_t t_pad, int ek, const void *wr, int E, int d, int T,
+                 const int32_t *toff, void *dx, bool accumulate, WsHeader *hdr, cudaStream_t s) {
+  using namespace tc;
+  CUtensorMap mA, mB, mC;
+  if (!make_map(&mA, dl16, t_pad, ek, 128) || !make_map(&mB, wr, E, d, MN_BOX) || !make_store_map(&mC, dx, T, d))
+    return MOE_ERR_CUDA;
+  Params p{};
+  p.tile_offsets = toff;
+  p.hdr = hdr;
+  p.E = 1;
+  p.d = d;
+  p.n_tiles = (d + BN - 1) / BN;
+  p.num_kb = ek / BK;
+  p.b_rows_e = 0;
+  p.out0 = (__nv_bfloat16 *)dx;
+  p.ld0 = d;
+  p.aux = accumulate ? (const __nv_bfloat16 *)dx : nullptr;
+  p.ld_aux = d;
+  p.rows_valid = T;
+  return launch_single<RDX>(mA, mB, mC, mC, p, (t_pad / BM) * p.n_tiles, s);
+}
+
+// fp32 partials part[g] = dL_g^T x_g for the G token ranges of toff_split (in 128-row tiles).
+int tc_router_dw(const void *dl16, int64_t t_pad, int ek, const void *x, int T, int d, int E,
+                 const int32_t *toff_split, int G, float *part, WsHeader *hdr, cudaStream_t s) {
+  using namespace tc;
+  CUtensorMap mA, mB;
+  if (!make_map(&mA, dl16, t_pad, ek, MN_BOX) || !make_map(&mB, x, T, d, MN_BOX)) return MOE_ERR_CUDA;
+  Params p{};
+  p.tile_offsets = toff_split;
+  p.hdr = hdr;
+  p.E = G;
+  p.d = d;
+  p.m_tiles = (E + BM - 1) / BM;
+  p.n_tiles = (d + BN - 1) / BN;
+  p.outf = part;
+  p.ldf = d;
+  p.rows_valid = E;
+  return launch_single<RDW>(mA, mB, mA, mA, p, (int64_t)G * p.m_tiles * p.n_tiles, s);
 }
 
 }  // namespace moe

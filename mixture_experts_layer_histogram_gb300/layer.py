@@ -2,6 +2,7 @@
 
 Forward (one stream, no host synchronisation):
   moe_route_topk   logits [T,E]        -> topk_idx [T,k], topk_w [T,k]
+   (or, given router weights: moe_router_fwd  x, w_router [E,d] -> logits, topk_idx, topk_w)
   moe_count_index  topk_idx            -> counts, offsets, tile_offsets, row_of_slot, token_of_row
   moe_permute      x [T,d]             -> x_perm [rows_max,d]
   moe_grouped_ffn_fwd                  -> ab [rows_max,2f], h [rows_max,f], y_perm [rows_max,d]
@@ -10,6 +11,7 @@ Backward:
   moe_combine_bwd  grad_out            -> dy_perm, d_topk_w [T,k], d_logits [T,E]
   moe_grouped_ffn_bwd                  -> dab, dx_perm, dw_gate_up [E,2f,d], dw_down [E,d,f]
   moe_combine_fwd  dx_perm, w = NULL   -> dx [T,d]      (backward of the permutation)
+  moe_router_bwd   d_logits            -> dx += d_logits w_router, dw_router [E,d]   (router layers)
 
 Every step runs in libmoe's kernels; this module only allocates buffers (PyTorch device memory)
 and calls the C ABI in order.
@@ -25,10 +27,12 @@ class MoELayer:
     """Buffers of one layer pass, allocated once and reused every step (no allocation per step)."""
 
     def __init__(self, T, d, E, k, f, dtype=torch.bfloat16, device="cuda", backward=True, recompute=False,
-                 scratch=None):
+                 scratch=None, router=False):
         """recompute: the backward recomputes ab and h from x_perm instead of reading them (selective
         activation checkpointing); ab and h may then live in `scratch` (a dict with tensors "ab" [R, 2f]
-        and "h" [R, f] shared with other layers)."""
+        and "h" [R, f] shared with other layers).
+        router: the layer computes its logits from x and router weights (forward(..., w_router=W_r)),
+        and its backward adds the router's share to dx and returns dw_router."""
         if not torch.cuda.is_available():
             raise RuntimeError("MoELayer needs a CUDA device")
         self.T, self.d, self.E, self.k, self.f = T, d, E, k, f
@@ -58,6 +62,14 @@ class MoELayer:
         self.y_perm = torch.empty((R, d), **act)
         self.out = torch.empty((T, d), **act)
         self.backward_enabled = backward
+        self.router = router
+        self._x = self._w_router = None
+        if router:
+            self.logits = torch.empty((T, E), dtype=torch.float32, device=self.device)
+            self.ws_router = torch.zeros(L.moe_router_workspace_size(T, d, E, L.dtype_code(dtype)), dtype=torch.uint8,
+                                         device=self.device)
+            if backward:
+                self.dw_router = torch.empty((E, d), **act)
         if backward:
             self.dy_perm = torch.empty((R, d), **act)
             self.dab = torch.empty((R, 2 * f), **act)
@@ -68,8 +80,17 @@ class MoELayer:
             self.dw_gate_up = torch.empty((E, 2 * f, d), **act)
             self.dw_down = torch.empty((E, d, f), **act)
 
-    def forward(self, x, logits, w_gate_up, w_down, stream=None):
-        L.moe_route_topk(logits, self.k, self.topk_idx, self.topk_w, stream)
+    def forward(self, x, logits, w_gate_up, w_down, stream=None, w_router=None):
+        """logits [T, E] fp32, or None with w_router [E, d] on a router layer (logits = x w_router^T,
+        fused with the top-k selection)."""
+        if w_router is not None:
+            if not self.router or logits is not None:
+                raise ValueError("w_router needs a layer built with router=True and logits=None")
+            L.moe_router_fwd(x, w_router, self.k, self.logits, self.topk_idx, self.topk_w, self.ws_router, stream)
+            self._x, self._w_router = x, w_router
+        else:
+            L.moe_route_topk(logits, self.k, self.topk_idx, self.topk_w, stream)
+            self._x = self._w_router = None
         L.moe_count_index(self.topk_idx, self.E, self.counts, self.offsets, self.tile_offsets, self.row_of_slot,
                           self.token_of_row, self.ws_index, stream)
         L.moe_permute(x, self.k, self.E, self.row_of_slot, self.counts, self.tile_offsets, self.x_perm, stream)
@@ -87,14 +108,23 @@ class MoELayer:
         bwd(self.dy_perm, self.x_perm, self.ab, self.h, w_gate_up, w_down, self.tile_offsets, self.dab, self.dx_perm,
             self.dw_gate_up, self.dw_down, self.ws_ffn, stream)
         L.moe_combine_fwd(self.dx_perm, None, self.row_of_slot, self.T, self.k, self.dx, stream)
-        return dict(dx=self.dx, d_logits=self.d_logits, d_topk_w=self.d_topk_w, dw_gate_up=self.dw_gate_up,
-                    dw_down=self.dw_down)
+        res = dict(dx=self.dx, d_logits=self.d_logits, d_topk_w=self.d_topk_w, dw_gate_up=self.dw_gate_up,
+                   dw_down=self.dw_down)
+        if self._w_router is not None:
+            L.moe_router_bwd(self._x, self._w_router, self.d_logits, self.dx, self.dw_router, self.ws_router,
+                             accumulate_dx=True, stream=stream)
+            res["dw_router"] = self.dw_router
+        return res
 
     def status(self, stream=None):
-        """Device status words (synchronises): (count_index, grouped_ffn)."""
-        return L.moe_read_status(self.ws_index, stream), L.moe_read_status(self.ws_ffn, stream)
+        """Device status words (synchronises): (count_index, grouped_ffn), plus the router's on a router layer."""
+        st = (L.moe_read_status(self.ws_index, stream), L.moe_read_status(self.ws_ffn, stream))
+        return st + (L.moe_read_status(self.ws_router, stream),) if self.router else st
 
     # kernels launched per pass, for the bench's launch count
     def launches(self, backward=True):
         fwd = 1 + 2 + 1 + 2 + 1
-        return fwd + ((1 + 4 + 1 + (1 if self.recompute else 0)) if backward else 0)
+        bwd = 1 + 4 + 1 + (1 if self.recompute else 0)
+        if self._w_router is not None:
+            bwd += 4   # prep, dx GEMM, dW GEMM, reduce
+        return fwd + (bwd if backward else 0)

@@ -57,6 +57,10 @@ def test_rows_max_and_workspace_sizes(L):
     assert _lib.moe_count_index_workspace_size(16384, 8, 64) >= 64 + 256 + 256 + 128 * 64 * 8
     assert _lib.moe_count_index_hook_offset(64) % 16 == 0
     assert _lib.moe_grouped_ffn_workspace_size(64, 2048, 1024, 139264, 1, 1) >= 4
+    # router: header + bf16 copy of d_logits (8192 x 64) + fp32 partials of at least one token range
+    assert _lib.moe_router_workspace_size(8192, 2048, 64, 1) >= 256 + 8192 * 64 * 2 + 64 * 2048 * 4
+    assert _lib.moe_router_workspace_size(256, 64, 8, 0) >= 256 + 256 * 8 * 4
+    assert _lib.moe_router_workspace_size(0, 64, 8, 1) >= 256
 
 
 FAKE = ctypes.c_void_p(1 << 20)   # never dereferenced: every call below fails validation first
@@ -90,6 +94,19 @@ def test_invalid_arguments_are_rejected_on_the_host(L):
     assert L.moe_combine_fwd(FAKE, FAKE, FAKE, 64, 64, 2, rm, 1, ctypes.c_void_p((1 << 20) + 2), NULL) == -1
     assert L.moe_combine_fwd(FAKE, FAKE, FAKE, 64, 64, 0, rm, 1, FAKE, NULL) == -1
     assert L.moe_combine_bwd(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 64, 64, 9, 8, rm, 1, FAKE, FAKE, FAKE, NULL) == -1
+    # router: k > E, E too large, bf16 d not a multiple of 8, workspace too small or misaligned, nulls
+    rws = L.moe_router_workspace_size(64, 256, 8, 1)
+    assert L.moe_router_fwd(FAKE, FAKE, 64, 256, 8, 9, 1, FAKE, FAKE, FAKE, FAKE, rws, NULL) == -1
+    assert L.moe_router_fwd(FAKE, FAKE, 64, 256, 300, 2, 1, FAKE, FAKE, FAKE, FAKE, rws, NULL) == -1
+    assert L.moe_router_fwd(FAKE, FAKE, 64, 252, 8, 2, 1, FAKE, FAKE, FAKE, FAKE, rws, NULL) == -2
+    assert L.moe_router_fwd(FAKE, FAKE, 64, 256, 8, 2, 1, FAKE, FAKE, FAKE, FAKE, rws - 1, NULL) == -1
+    assert L.moe_router_fwd(FAKE, FAKE, 64, 256, 8, 2, 1, FAKE, FAKE, FAKE, ctypes.c_void_p((1 << 20) + 16), rws,
+                            NULL) == -1
+    assert L.moe_router_fwd(FAKE, NULL, 64, 256, 8, 2, 1, FAKE, FAKE, FAKE, FAKE, rws, NULL) == -1
+    assert L.moe_router_fwd(FAKE, FAKE, 64, 256, 8, 2, 1, ctypes.c_void_p((1 << 20) + 4), FAKE, FAKE, FAKE, rws,
+                            NULL) == -1
+    assert L.moe_router_bwd(FAKE, FAKE, FAKE, 64, 256, 8, 1, 0, FAKE, NULL, FAKE, rws, NULL) == -1
+    assert L.moe_router_bwd(FAKE, FAKE, FAKE, 64, 256, 8, 2, 0, FAKE, FAKE, FAKE, rws, NULL) == -1
     assert L.moe_read_status(NULL, NULL) == -1
 
 
