@@ -133,20 +133,25 @@ def run_ours(args):
     x, logits, wgu, wd = inp["x"], inp["logits"], inp["w_gate_up"], inp["w_down"]
     g = inp.get("g")
     bwd = w.backward
-    layer = MoELayer(w.T, w.d, w.E, w.k, w.f, w.torch_dtype, dev, backward=bwd, recompute=args.recompute)
+    layer = MoELayer(w.T, w.d, w.E, w.k, w.f, w.torch_dtype, dev, backward=bwd, recompute=args.recompute,
+                     router=args.router)
+    wr = moe_inputs.make_router_weight(w, dev) if args.router else None
     stream = torch.cuda.current_stream(dev)
     M = w.T * w.k
     gemm_flop = (18.0 if bwd else 6.0) * M * w.d * w.f
 
     def step(ev=None):
         if ev is None:
-            layer.forward(x, logits, wgu, wd)
+            layer.forward(x, None if args.router else logits, wgu, wd, w_router=wr)
             if bwd:
                 layer.backward(g, wgu, wd)
             return
         # events around each C-ABI call, on the stream the kernels are launched on
         ev[0].record(stream)
-        L.moe_route_topk(logits, w.k, layer.topk_idx, layer.topk_w)
+        if args.router:
+            L.moe_router_fwd(x, wr, w.k, layer.logits, layer.topk_idx, layer.topk_w, layer.ws_router)
+        else:
+            L.moe_route_topk(logits, w.k, layer.topk_idx, layer.topk_w)
         ev[1].record(stream)
         L.moe_count_index(layer.topk_idx, w.E, layer.counts, layer.offsets, layer.tile_offsets, layer.row_of_slot,
                           layer.token_of_row, layer.ws_index)
@@ -159,9 +164,8 @@ def run_ours(args):
         L.moe_combine_fwd(layer.y_perm, layer.topk_w, layer.row_of_slot, w.T, w.k, layer.out)
         ev[5].record(stream)
         if not bwd:
-            ev[6].record(stream)
-            ev[7].record(stream)
-            ev[8].record(stream)
+            for j in range(6, 10):
+                ev[j].record(stream)
             return
         L.moe_combine_bwd(g, layer.y_perm, layer.topk_w, layer.topk_idx, layer.row_of_slot, layer.counts,
                           layer.tile_offsets, w.E, layer.dy_perm, layer.d_topk_w, layer.d_logits)
@@ -172,18 +176,21 @@ def run_ours(args):
         ev[7].record(stream)
         L.moe_combine_fwd(layer.dx_perm, None, layer.row_of_slot, w.T, w.k, layer.dx)
         ev[8].record(stream)
+        if args.router:
+            L.moe_router_bwd(x, wr, layer.d_logits, layer.dx, layer.dw_router, layer.ws_router, accumulate_dx=True)
+        ev[9].record(stream)
 
     clk = ClockSampler(dev.index).start()
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize(dev)
     st = layer.status()
-    if st != (0, 0):
+    if any(st):
         raise RuntimeError(f"device status after warm-up: {st}")
 
-    names = ["route_topk", "count_index", "permute", "grouped_ffn_fwd", "combine_fwd", "combine_bwd",
-             "grouped_ffn_bwd", "unpermute"]
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(9)] for _ in range(args.steps)]
+    names = ["router_fwd" if args.router else "route_topk", "count_index", "permute", "grouped_ffn_fwd",
+             "combine_fwd", "combine_bwd", "grouped_ffn_bwd", "unpermute", "router_bwd"]
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(10)] for _ in range(args.steps)]
     t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     if world > 1:
         dist.barrier()
@@ -206,19 +213,21 @@ def run_ours(args):
     per = {n: statistics.mean(evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(args.steps))
            for j, n in enumerate(names)}
     st = layer.status()
-    if st != (0, 0):
+    if any(st):
         raise RuntimeError(f"device status after timing: {st}")
 
     # ---------------------------------------------------------------- end to end: host buffers
     # Every step uploads its inputs from pinned host memory and downloads its results through the
     # public host-buffer pipeline; uploads and downloads overlap the neighbouring steps' compute.
-    pin = dict(x=x.cpu().pin_memory(), logits=logits.cpu().pin_memory())
+    pin = dict(x=x.cpu().pin_memory())
+    if not args.router:
+        pin["logits"] = logits.cpu().pin_memory()
     if bwd:
         pin["g"] = g.cpu().pin_memory()
     pipe = HostPipeline(layer)
     h2d, d2h = pipe.h2d_bytes(), pipe.d2h_bytes()
     for i in range(3):
-        pipe.submit(pin, wgu, wd, next_batch=pin if i < 2 else None)
+        pipe.submit(pin, wgu, wd, next_batch=pin if i < 2 else None, w_router=wr)
     pipe.join()
     torch.cuda.synchronize(dev)
     if world > 1:
@@ -227,7 +236,7 @@ def run_ours(args):
     e0.record(stream)
     pipe.h2d.wait_stream(stream)
     for i in range(args.steps):
-        pipe.submit(pin, wgu, wd, next_batch=pin if i + 1 < args.steps else None)
+        pipe.submit(pin, wgu, wd, next_batch=pin if i + 1 < args.steps else None, w_router=wr)
     pipe.join()
     e1.record(stream)
     torch.cuda.synchronize(dev)
@@ -237,7 +246,7 @@ def run_ours(args):
         dist.all_reduce(tt, op=dist.ReduceOp.MAX)
         e2e_ms = float(tt.item())
     st = layer.status()
-    if st != (0, 0):
+    if any(st):
         raise RuntimeError(f"device status after the end-to-end run: {st}")
 
     cpu_base = None
@@ -259,8 +268,13 @@ def run_ours(args):
         "combine_fwd": (M * w.d + w.T * w.d) * es + M * 8,
         "combine_bwd": (w.T * w.d + 2 * M * w.d) * es + M * 16 + w.T * w.E * 4,
         "unpermute": (M * w.d + w.T * w.d) * es + M * 4,
+        # router: x and Wr read, logits and the selection written; backward: d_logits, x, Wr read,
+        # dx read and written (accumulated), dWr written
+        "router_fwd": (w.T * w.d + w.E * w.d) * es + w.T * w.E * 4 + w.T * w.k * 8,
+        "router_bwd": (3 * w.T * w.d + 2 * w.E * w.d) * es + w.T * w.E * 4,
     }
-    kern = {n: {"ms": round(v, 4)} for n, v in per.items() if bwd or n in names[:5]}
+    kern = {n: {"ms": round(v, 4)} for n, v in per.items()
+            if (bwd or n in names[:5]) and (args.router or n != "router_bwd")}
     for n, b in mem_bytes.items():
         if n not in kern:
             continue
@@ -288,7 +302,8 @@ def run_ours(args):
         "warmup": args.warmup, "ms_per_step": round(ms, 4), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": w.dtype, "data": "synthetic (seeded; see moe_inputs.py)",
         "config": {"workload": w.name, "T": w.T, "d": w.d, "E": w.E, "k": w.k, "f": w.f, "routing": w.routing,
-                   "pass": ("fwd+bwd (recompute)" if args.recompute else "fwd+bwd") if bwd else "fwd",
+                   "pass": (("fwd+bwd (recompute)" if args.recompute else "fwd+bwd") if bwd else "fwd") +
+                           (", router GEMM in the pass" if args.router else ""),
                    "parallelism": f"replicas x{world}",
                    "l2": "inputs larger than L2 (expert weights 768 MiB, grouped activations > 129 MB); no flush"},
         "roofline": roofline,
@@ -376,6 +391,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--router", action="store_true",
+                    help="the pass starts from x and router weights: router GEMM with fused top-k, and its backward")
     ap.add_argument("--recompute", action="store_true",
                     help="backward recomputes ab, h from x_perm (selective activation checkpointing)")
     ap.add_argument("--ref-tokens", type=int, default=8)

@@ -49,6 +49,9 @@ constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 32 * 32 * 2 * 2 * EPI_WARPS + 
 enum Kind { GATEUP = 0, DOWN = 1, DH = 2, DGRAD = 3, WGRAD = 4, RDX = 5, RDW = 6 };
 // kinds whose tiles reduce over the rows of one group (A and B read MN-major)
 __host__ __device__ constexpr bool row_reduce(int kind) { return kind == WGRAD || kind == RDW; }
+// 16-byte vectors an epilogue thread loads before its accumulator is ready: DH the first chunk of
+// a and b, RDX its row's whole addend (128 columns)
+__host__ __device__ constexpr int pre_count(int kind) { return kind == RDX ? 16 : 8; }
 
 struct Params {
   const int32_t *tile_offsets;
@@ -160,7 +163,7 @@ struct EpiStore {
 // is this thread's row in the tile, `yrow` the global row (in the output map) of the warp's first row.
 template <int KIND>
 __device__ __forceinline__ void epilogue_tile(const Tile &t, const Params &p, uint32_t tbase, int row, int yrow, int c0,
-                                              const uint4 (&pre)[8], EpiStore &es, const CUtensorMap *mc0,
+                                              const uint4 (&pre)[pre_count(KIND)], EpiStore &es, const CUtensorMap *mc0,
                                               const CUtensorMap *mc1) {
   float v[32];
   uint32_t r[32];
@@ -239,18 +242,23 @@ __device__ __forceinline__ void epilogue_tile(const Tile &t, const Params &p, ui
       }
     }
   } else {
-    // RDX with an addend: this row's previous dx (rows past the tokens and columns past d are not
-    // read; the store map drops them)
-    const bool add = KIND == RDX && p.aux != nullptr && t.m0 + row < p.rows_valid;
-    const __nv_bfloat16 *arow = add ? p.aux + (int64_t)(t.m0 + row) * p.ld_aux + t.n0 : nullptr;
+    // RDX: with an addend, this row's previous dx, loaded in full (pre) before the accumulator was
+    // ready (zeros past the tokens and past d)
+    const bool add = KIND == RDX && p.aux != nullptr;
+    if (KIND != RDX) {
 #pragma unroll 1
-    for (int c = c0; c < c0 + BN / 2; c += 32) {
-      uint4 q[4] = {};
-      if (KIND == RDX && add) {
+      for (int c = c0; c < c0 + BN / 2; c += 32) {
+        tmem_ld32(tbase + c, r);
+        tmem_ld_wait();
 #pragma unroll
-        for (int i = 0; i < 4; ++i)
-          if (t.n0 + c + 8 * i < p.d) q[i] = *reinterpret_cast<const uint4 *>(arow + c + 8 * i);
+        for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+        es.put(mc0, t.n0 + c, yrow, v);
       }
+      return;
+    }
+#pragma unroll
+    for (int cc = 0; cc < BN / 64; ++cc) {
+      const int c = c0 + 32 * cc;
       tmem_ld32(tbase + c, r);
       tmem_ld_wait();
 #pragma unroll
@@ -258,7 +266,7 @@ __device__ __forceinline__ void epilogue_tile(const Tile &t, const Params &p, ui
       if (KIND == RDX && add) {
         float av[32];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) unpack_bf16x8(q[i], av + 8 * i);
+        for (int i = 0; i < 4; ++i) unpack_bf16x8(pre[(4 * cc + i) % pre_count(KIND)], av + 8 * i);
 #pragma unroll
         for (int i = 0; i < 32; ++i) v[i] += av[i];
       }
@@ -435,7 +443,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
         continue;
       }
-      uint4 pre[8];
+      uint4 pre[pre_count(KIND)];
       if (KIND == DH) {   // first chunk of a, b: independent of the MMA, load before waiting
         const __nv_bfloat16 *abrow = p.aux + (int64_t)(t.m0 + row_in_tile) * p.ld_aux + t.n0 + c0;
 #pragma unroll
@@ -443,6 +451,13 @@ __global__ void __launch_bounds__(THREADS, 1)
           pre[i] = reinterpret_cast<const uint4 *>(abrow)[i];
           pre[4 + i] = reinterpret_cast<const uint4 *>(abrow + p.f)[i];
         }
+      }
+      if (KIND == RDX && p.aux != nullptr) {   // the addend row: independent of the MMA as well
+        const bool live = t.m0 + row_in_tile < p.rows_valid;
+        const __nv_bfloat16 *arow = p.aux + (int64_t)(live ? t.m0 + row_in_tile : 0) * p.ld_aux + t.n0 + c0;
+#pragma unroll
+        for (int i = 0; i < pre_count(KIND); ++i)
+          pre[i] = (live && t.n0 + c0 + 8 * i < p.d) ? reinterpret_cast<const uint4 *>(arow)[i] : make_uint4(0, 0, 0, 0);
       }
       if (!mbar_wait(tfull_bar(acc), acc_phase, abort_flag, p.hdr, 4)) break;
       tc_fence_after();
@@ -832,7 +847,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
         }
         continue;
       }
-      uint4 pre[8];
+      uint4 pre[pre_count(KIND)];
       if (KIND == DH) {   // the next tile's a, b rows of this thread: into L2 now, read one tile later
         const int nxt = tile + num_clusters;
         if (nxt < num_tiles) {

@@ -10,10 +10,15 @@
 //               a ring of up to 8 stages
 //   warp 1      allocates TMEM (two accumulators of 128 lanes x E columns), issues tcgen05.mma
 //               with M = 128 tokens, N = E rounded up to 16 (rows of Wr past E read as zero)
-//   warps 2..5  epilogue, one thread per token: tcgen05.ld of the token's E logits, 32 at a time,
-//               optional store of the fp32 logits, insertion into a sorted top-k list held in
-//               registers (value desc, id asc), softmax of the selected logits
-// The logits never make a round trip through HBM (x is read once, Wr stays in L2).
+//   warps 2..9  epilogue, two threads per token (warps 2..5 and 6..9 share the TMEM lane quarters
+//               and split the columns): tcgen05.ld of the token's logits, 32 at a time, optional
+//               store of the fp32 logits, insertion into a sorted top-k list held in registers
+//               (value desc, id asc); the two lists merge through shared memory, then the softmax
+//               of the selected logits
+// When there are fewer token tiles than SMs, S (<= 4) CTAs share a tile, each over 1/S of d: each
+// writes fp32 partial logits to the workspace and the last one to finish (an atomic count per tile)
+// adds the S partials in split order (deterministic) and selects. x is read once either way; Wr
+// stays in L2.
 //
 // bf16 backward: router_prep_kernel writes dl16 = bf16(dL) [t_pad, ek] with zero padding and the
 // group offsets; the single-CTA grouped-GEMM kernel runs its RDX kind (dx (+)= dl16 Wr) and its
@@ -38,13 +43,14 @@ using namespace tc;
 
 constexpr int RBM = 128;                 // tokens per tile (TMEM lanes)
 constexpr int RBK = 64;                  // k depth of one stage (128 B of bf16: the swizzle span)
-constexpr int R_THREADS = 192;           // warp 0 TMA, warp 1 MMA, warps 2..5 epilogue
-constexpr int R_EPI_THREADS = 128;
+constexpr int R_THREADS = 320;           // warp 0 TMA, warp 1 MMA, warps 2..9 epilogue
+constexpr int R_EPI_THREADS = 256;       // two threads per token: each takes half of the experts
 constexpr int R_A_BYTES = RBM * RBK * 2; // 16 KB
 constexpr int R_RING_BYTES = 192 * 1024;
 constexpr int R_MAX_STAGES = 8;
-constexpr int R_SMEM = R_RING_BYTES + 1024 + 8 * (2 * R_MAX_STAGES + 5) + 16;
-constexpr int kSplitTarget = 296;        // RDW: aim for about this many output tiles (2 per SM)
+constexpr int R_MERGE_BYTES = RBM * MOE_MAX_TOPK * 8;   // upper-half top-k lists handed to the lower half
+constexpr int R_SMEM = R_RING_BYTES + R_MERGE_BYTES + 1024 + 8 * (2 * R_MAX_STAGES + 5) + 16;
+constexpr int kSplitTarget = 152;        // RDW: aim for about one output tile per SM
 constexpr int kMaxSplits = 64;
 
 struct FwdParams {
@@ -56,30 +62,68 @@ struct FwdParams {
   int stage_bytes;
   int num_kb;      // ceil(d / 64)
   int num_tiles;   // ceil(T / 128)
+  int splits;      // S: CTAs that share one token tile, each over kb_split k-blocks of d
+  int kb_split;
+  float *partial;          // S > 1: fp32 partial logits [S, T, E]
+  uint32_t *tile_count;    // S > 1: per-tile count of finished splits (zero at launch)
   float *logits;   // may be null
   int32_t *topk_idx;
   float *topk_w;
 };
 
-// Insert (v, e) into the list tv/ti (k entries, sorted by value desc then id asc). Ids arrive in
-// increasing order, so an equal value goes after the entries already present; every entry after
-// the insertion point shifts down one place and the last one drops out.
+// Insert (v, e) into the list tv/ti (sorted by value desc, then id asc). Ids arrive in increasing
+// order, so v goes after every entry >= v, the entries after it shift down one place and the last
+// one drops out. Every slot's new content is computed from the old list at once (one comparison
+// per slot), which keeps the dependent chain per insertion short.
 template <int KMAX>
-__device__ __forceinline__ void topk_insert(float (&tv)[KMAX], int (&ti)[KMAX], int k, float v, int e) {
-  float cv = v;
-  int ci = e;
-  bool shifting = false;
+__device__ __forceinline__ void topk_insert(float (&tv)[KMAX], int (&ti)[KMAX], float v, int e) {
+  bool ge[KMAX];
 #pragma unroll
-  for (int j = 0; j < KMAX; ++j) {
-    const bool take = j < k && (shifting || cv > tv[j]);
-    const float ov = tv[j];
-    const int oi = ti[j];
-    tv[j] = take ? cv : ov;
-    ti[j] = take ? ci : oi;
-    cv = take ? ov : cv;
-    ci = take ? oi : ci;
-    shifting = shifting || take;
+  for (int j = 0; j < KMAX; ++j) ge[j] = tv[j] >= v;
+#pragma unroll
+  for (int j = KMAX - 1; j >= 0; --j) {
+    const bool prev_ge = j == 0 ? true : ge[j > 0 ? j - 1 : 0];
+    const float pv = j == 0 ? v : tv[j > 0 ? j - 1 : 0];
+    const int pi = j == 0 ? e : ti[j > 0 ? j - 1 : 0];
+    tv[j] = ge[j] ? tv[j] : (prev_ge ? v : pv);
+    ti[j] = ge[j] ? ti[j] : (prev_ge ? e : pi);
   }
+}
+
+// True on every epilogue thread (the 256 threads of warps 2..9) if `v` holds on any of them.
+__device__ __forceinline__ bool epi_any(bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.or.pred q, 1, %2, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"((uint32_t)v), "n"(R_EPI_THREADS)
+      : "memory");
+  return r != 0;
+}
+
+// One token's logits for columns [c0, c0 + 32): optional store of the fp32 logits, then insertion
+// into the top-k list.
+template <int KMAX>
+__device__ __forceinline__ void take_chunk(const float (&v)[32], int c0, int E, bool live, float *lrow, bool vec,
+                                           float (&tv)[KMAX], int (&ti)[KMAX]) {
+  if (live && lrow) {
+    if (vec) {
+#pragma unroll
+      for (int q = 0; q < 8; ++q)
+        if (c0 + 4 * q < E)
+          *reinterpret_cast<float4 *>(lrow + c0 + 4 * q) = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+    } else {
+#pragma unroll
+      for (int i = 0; i < 32; ++i)
+        if (c0 + i < E) lrow[c0 + i] = v[i];
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < 32; ++i)
+    if (c0 + i < E) topk_insert<KMAX>(tv, ti, v[i], c0 + i);
 }
 
 template <int KMAX>
@@ -89,10 +133,13 @@ __global__ void __launch_bounds__(R_THREADS, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int S = p.stages;
-  uint64_t *bars = reinterpret_cast<uint64_t *>(smem + R_RING_BYTES);
+  float *merge_v = reinterpret_cast<float *>(smem + R_RING_BYTES);            // [MOE_MAX_TOPK][RBM]
+  int *merge_i = reinterpret_cast<int *>(smem + R_RING_BYTES + R_MERGE_BYTES / 2);
+  uint64_t *bars = reinterpret_cast<uint64_t *>(smem + R_RING_BYTES + R_MERGE_BYTES);
   // bars: full[S], empty[S], tfull[2], tempty[2], mma_done
   uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(bars + 2 * R_MAX_STAGES + 5);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_holder + 1);
+  volatile int *last_flag = abort_flag + 1;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t sbase = smem_u32(smem);
@@ -103,6 +150,8 @@ __global__ void __launch_bounds__(R_THREADS, 1)
   auto tempty_bar = [&](int a) { return bar0 + 8u * (2 * R_MAX_STAGES + 2 + a); };
   const uint32_t mma_done_bar = bar0 + 8u * (2 * R_MAX_STAGES + 4);
   const uint32_t tmem_cols = 2u * (uint32_t)p.acc_cols;
+  const int splits = p.splits;
+  const int num_units = p.num_tiles * splits;   // unit u: tile u / splits, split u % splits
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
@@ -115,6 +164,7 @@ __global__ void __launch_bounds__(R_THREADS, 1)
     }
     mbar_init(mma_done_bar, 1);
     *abort_flag = 0;
+    *last_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmX)) : "memory");
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmW)) : "memory");
@@ -135,8 +185,10 @@ __global__ void __launch_bounds__(R_THREADS, 1)
     int stage = 0;
     uint32_t phase = 0, issued = 0;
     bool ok = true;
-    for (int tile = blockIdx.x; tile < p.num_tiles && ok; tile += gridDim.x) {
-      for (int kb = 0; kb < p.num_kb; ++kb) {
+    for (int u = blockIdx.x; u < num_units && ok; u += gridDim.x) {
+      const int tile = u / splits, kb0 = (u - tile * splits) * p.kb_split;
+      const int kb1 = min(p.num_kb, kb0 + p.kb_split);
+      for (int kb = kb0; kb < kb1; ++kb) {
         if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag, p.hdr, 11)) { ok = false; break; }
         const uint32_t sA = sbase + stage * p.stage_bytes, fb = full_bar(stage);
         mbar_expect_tx(fb, p.stage_bytes);
@@ -160,18 +212,20 @@ __global__ void __launch_bounds__(R_THREADS, 1)
     int stage = 0, acc = 0;
     uint32_t phase = 0, acc_phase = 0;
     bool issued_any = false, ok = true;
-    for (int tile = blockIdx.x; tile < p.num_tiles && ok; tile += gridDim.x) {
+    for (int u = blockIdx.x; u < num_units && ok; u += gridDim.x) {
+      const int tile = u / splits, kb0 = (u - tile * splits) * p.kb_split;
+      const int kb1 = min(p.num_kb, kb0 + p.kb_split);
       if (!mbar_wait(tempty_bar(acc), acc_phase ^ 1u, abort_flag, p.hdr, 12)) break;
       tc_fence_after();
       const uint32_t d_tmem = tmem_base + (uint32_t)(acc * p.acc_cols);
-      for (int kb = 0; kb < p.num_kb; ++kb) {
+      for (int kb = kb0; kb < kb1; ++kb) {
         if (!mbar_wait(full_bar(stage), phase, abort_flag, p.hdr, 13)) { ok = false; break; }
         tc_fence_after();
         const uint32_t sA = sbase + stage * p.stage_bytes, sB = sA + R_A_BYTES;
 #pragma unroll
         for (int kk = 0; kk < RBK / 16; ++kk)
           mma_bf16(d_tmem, sdesc(sA + kk * 32, 16, 1024), sdesc(sB + kk * 32, 16, 1024), idesc,
-                   (kb | kk) != 0 ? 1u : 0u);
+                   (kb != kb0 || kk != 0) ? 1u : 0u);
         issued_any = true;
         mma_commit(empty_bar(stage));
         if (++stage == S) { stage = 0; phase ^= 1u; }
@@ -187,19 +241,28 @@ __global__ void __launch_bounds__(R_THREADS, 1)
       while (!mbar_try_wait(mma_done_bar, 0) && global_ns() - t0 < kWaitLimitNs) {}
     }
   } else if (warp >= 2) {
-    // ------------------------------------------------------------------ epilogue: one token per thread
+    // ------------------------------------------------------------------ epilogue: two threads per token
+    // Warps 2..5 (half 0) and 6..9 (half 1) share the TMEM lane quarters; in each pair the thread
+    // of half h takes the 32-column chunks [h * nc0, ...) of its token's logits, keeps its own
+    // top-k list, and half 1 hands its list to half 0 through shared memory for the final merge.
     const int quarter = warp & 3;   // TMEM lanes 32 * quarter ... 32 * quarter + 31
+    const int half = (warp - 2) >> 2;
     const int row = quarter * 32 + lane;
     const int E = p.E, k = p.k;
+    const int nc = (E + 31) / 32, nc0 = (nc + 1) / 2;
+    const int cbeg = half ? nc0 * 32 : 0, cend = half ? E : (nc0 * 32 < E ? nc0 * 32 : E);
     const bool vec = (E & 3) == 0;
     int acc = 0;
     uint32_t acc_phase = 0;
-    for (int tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x) {
-      if (!mbar_wait(tfull_bar(acc), acc_phase, abort_flag, p.hdr, 14)) break;
+    for (int u = blockIdx.x; u < num_units; u += gridDim.x) {
+      const int tile = u / splits, split = u - tile * splits;
+      const bool got = mbar_wait(tfull_bar(acc), acc_phase, abort_flag, p.hdr, 14);
+      if (epi_any(!got)) break;   // all epilogue threads leave together: they meet at named barriers
       tc_fence_after();
       const int t = tile * RBM + row;
       const bool live = t < p.T;
       const uint32_t tbase = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * p.acc_cols);
+      float *lrow = p.logits ? p.logits + (int64_t)t * E : nullptr;
       float tv[KMAX];
       int ti[KMAX];
 #pragma unroll
@@ -207,35 +270,109 @@ __global__ void __launch_bounds__(R_THREADS, 1)
         tv[j] = -INFINITY;
         ti[j] = 0;
       }
-      float *lrow = p.logits ? p.logits + (int64_t)t * E : nullptr;
+      bool last = true;
+      if (splits == 1) {
 #pragma unroll 1
-      for (int c0 = 0; c0 < E; c0 += 32) {
-        uint32_t r[32];
-        tmem_ld32(tbase + c0, r);
-        tmem_ld_wait();
-        if (live && lrow) {
-          if (vec) {
+        for (int c0 = cbeg; c0 < cend; c0 += 32) {
+          uint32_t r[32];
+          float v[32];
+          tmem_ld32(tbase + c0, r);
+          tmem_ld_wait();
 #pragma unroll
-            for (int q = 0; q < 8; ++q)
-              if (c0 + 4 * q < E)
-                *reinterpret_cast<float4 *>(lrow + c0 + 4 * q) =
-                    make_float4(__uint_as_float(r[4 * q]), __uint_as_float(r[4 * q + 1]),
-                                __uint_as_float(r[4 * q + 2]), __uint_as_float(r[4 * q + 3]));
-          } else {
+          for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+          take_chunk<KMAX>(v, c0, E, live, lrow, vec, tv, ti);
+        }
+        tc_fence_before();
+        mbar_arrive(tempty_bar(acc));
+      } else {
+        // this split's partial logits -> global; the last split of the tile to finish adds all
+        // partials in split order and selects
+        float *prow = p.partial + ((int64_t)split * p.T + t) * E;
+#pragma unroll 1
+        for (int c0 = cbeg; c0 < cend; c0 += 32) {
+          uint32_t r[32];
+          tmem_ld32(tbase + c0, r);
+          tmem_ld_wait();
+          if (live) {
+            if (vec) {
 #pragma unroll
-            for (int i = 0; i < 32; ++i)
-              if (c0 + i < E) lrow[c0 + i] = __uint_as_float(r[i]);
+              for (int q = 0; q < 8; ++q)
+                if (c0 + 4 * q < E)
+                  *reinterpret_cast<float4 *>(prow + c0 + 4 * q) =
+                      make_float4(__uint_as_float(r[4 * q]), __uint_as_float(r[4 * q + 1]),
+                                  __uint_as_float(r[4 * q + 2]), __uint_as_float(r[4 * q + 3]));
+            } else {
+#pragma unroll
+              for (int i = 0; i < 32; ++i)
+                if (c0 + i < E) prow[c0 + i] = __uint_as_float(r[i]);
+            }
           }
         }
+        tc_fence_before();
+        mbar_arrive(tempty_bar(acc));
+        __threadfence();
+        asm volatile("bar.sync 1, %0;" ::"n"(R_EPI_THREADS) : "memory");
+        if (warp == 2 && lane == 0) {
+          const unsigned old = atomicAdd(p.tile_count + tile, 1u);
+          __threadfence();
+          *last_flag = old == (unsigned)(splits - 1);
+        }
+        asm volatile("bar.sync 1, %0;" ::"n"(R_EPI_THREADS) : "memory");
+        last = *last_flag != 0;
+        if (last) {
+#pragma unroll 1
+          for (int c0 = cbeg; c0 < cend; c0 += 32) {
+            float v[32];
 #pragma unroll
-        for (int i = 0; i < 32; ++i)
-          if (c0 + i < E) topk_insert<KMAX>(tv, ti, k, __uint_as_float(r[i]), c0 + i);
+            for (int i = 0; i < 32; ++i) v[i] = 0.0f;
+            if (live) {
+              if (vec) {
+#pragma unroll
+                for (int q = 0; q < 4; ++q)   // at most 4 splits; the loads of all of them can be in flight
+                  if (q < splits) {
+                    const float4 *src = reinterpret_cast<const float4 *>(p.partial + ((int64_t)q * p.T + t) * E + c0);
+#pragma unroll
+                    for (int j = 0; j < 8; ++j)
+                      if (c0 + 4 * j < E) {
+                        const float4 f = __ldcg(src + j);
+                        v[4 * j] += f.x;
+                        v[4 * j + 1] += f.y;
+                        v[4 * j + 2] += f.z;
+                        v[4 * j + 3] += f.w;
+                      }
+                  }
+              } else {
+                for (int q = 0; q < splits; ++q) {
+                  const float *src = p.partial + ((int64_t)q * p.T + t) * E + c0;
+#pragma unroll
+                  for (int i = 0; i < 32; ++i)
+                    if (c0 + i < E) v[i] += __ldcg(src + i);
+                }
+              }
+            }
+            take_chunk<KMAX>(v, c0, E, live, lrow, vec, tv, ti);
+          }
+        }
       }
-      tc_fence_before();
-      mbar_arrive(tempty_bar(acc));
       acc ^= 1;
       if (acc == 0) acc_phase ^= 1u;
-      if (live) {
+      if (!last) continue;   // uniform across the epilogue threads
+      // merge: half 1 hands its list to half 0 (its experts have the higher ids, and its list is in
+      // (value desc, id asc) order, so inserting it entry by entry keeps the tie rule)
+      if (half == 1) {
+#pragma unroll
+        for (int j = 0; j < KMAX; ++j) {
+          merge_v[j * RBM + row] = tv[j];
+          merge_i[j * RBM + row] = ti[j];
+        }
+      }
+      asm volatile("bar.sync 1, %0;" ::"n"(R_EPI_THREADS) : "memory");
+      if (half == 0) {
+#pragma unroll
+        for (int j = 0; j < KMAX; ++j) topk_insert<KMAX>(tv, ti, merge_v[j * RBM + row], merge_i[j * RBM + row]);
+      }
+      asm volatile("bar.sync 1, %0;" ::"n"(R_EPI_THREADS) : "memory");   // merge buffer free again
+      if (half == 0 && live) {
         const float m = tv[0];
         float ex[KMAX], s = 0.0f;
 #pragma unroll
@@ -295,12 +432,20 @@ __global__ void __launch_bounds__(256) router_reduce_kernel(const float *__restr
   const int64_t plane = (int64_t)E * d;
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n4; i += stride) {
     float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int g = 0; g < G; ++g) {
-      const float4 q = __ldg(reinterpret_cast<const float4 *>(part + g * plane) + i);
-      s.x += q.x;
-      s.y += q.y;
-      s.z += q.z;
-      s.w += q.w;
+    for (int g0 = 0; g0 < G; g0 += 8) {   // eight partials' loads in flight, added in split order
+      float4 q[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        q[j] = g0 + j < G ? __ldg(reinterpret_cast<const float4 *>(part + (g0 + j) * plane) + i)
+                          : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        if (g0 + j < G) {
+          s.x += q[j].x;
+          s.y += q[j].y;
+          s.z += q[j].z;
+          s.w += q[j].w;
+        }
     }
     __nv_bfloat162 lo = __floats2bfloat162_rn(s.x, s.y), hi = __floats2bfloat162_rn(s.z, s.w);
     uint2 o;
@@ -378,6 +523,27 @@ static int splits_of(int T, int d, int E) {
 }
 static size_t dl16_bytes(int T, int E) { return (size_t)round_up((int64_t)t_pad_of(T) * ek_of(E) * 2, 256); }
 
+// Forward: S CTAs share a token tile when there are few tiles, so that about one CTA per SM streams
+// x (S <= 4, each split at least one 64-wide k-block). Depends on the shape only.
+constexpr int kFwdCtaTarget = 152;
+static void fwd_splits(int T, int d, int *splits, int *kb_split) {
+  const int tiles = (int)(t_pad_of(T) / RBM), num_kb = (d + RBK - 1) / RBK;
+  int S = tiles > 0 ? kFwdCtaTarget / tiles : 1;
+  if (S > 4) S = 4;
+  if (S > num_kb) S = num_kb;
+  if (S < 1) S = 1;
+  const int kbs = (num_kb + S - 1) / S;
+  *kb_split = kbs;
+  *splits = (num_kb + kbs - 1) / kbs;
+}
+// forward scratch: [header 256 B][tile counters, padded to 256 B][partials S x T x E fp32]
+static size_t fwd_count_bytes(int T) { return (size_t)round_up(t_pad_of(T) / RBM * 4, 256); }
+static size_t fwd_ws_bytes(int T, int d, int E) {
+  int S, kbs;
+  fwd_splits(T, d, &S, &kbs);
+  return kHdrBytes + fwd_count_bytes(T) + (S > 1 ? (size_t)S * T * E * 4 : 0);
+}
+
 }  // namespace router
 }  // namespace moe
 
@@ -387,7 +553,9 @@ using namespace moe::router;
 extern "C" size_t moe_router_workspace_size(int T, int d, int E, int dtype) {
   if (T < 0 || d < 1 || E < 1) return 0;
   if (dtype == MOE_F32) return kHdrBytes + (size_t)round_up((int64_t)T * E * 4, 256);
-  return kHdrBytes + kToffBytes + dl16_bytes(T, E) + (size_t)splits_of(T, d, E) * E * d * 4;
+  const size_t bwd = kHdrBytes + kToffBytes + dl16_bytes(T, E) + (size_t)splits_of(T, d, E) * E * d * 4;
+  const size_t fwd = fwd_ws_bytes(T, d, E);
+  return bwd > fwd ? bwd : fwd;
 }
 
 static int check_router(const void *x, const void *wr, int T, int d, int E, int dtype, const void *ws,
@@ -407,7 +575,7 @@ template <int KMAX>
 static int launch_fwd(const CUtensorMap &mx, const CUtensorMap &mw, const FwdParams &p, cudaStream_t s) {
   MOE_TRY_CUDA(cudaFuncSetAttribute(router_fwd_kernel<KMAX>, cudaFuncAttributeMaxDynamicSharedMemorySize, R_SMEM));
   int grid = sm_count();
-  if (p.num_tiles < grid) grid = p.num_tiles;
+  if (p.num_tiles * p.splits < grid) grid = p.num_tiles * p.splits;
   router_fwd_kernel<KMAX><<<grid, R_THREADS, R_SMEM, s>>>(mx, mw, p);
   MOE_CHECK_LAUNCH();
   return MOE_OK;
@@ -423,7 +591,8 @@ extern "C" int moe_router_fwd(const void *x, const void *w_router, int T, int d,
   if (logits && !aligned16(logits)) return MOE_ERR_INVALID_ARG;
   cudaStream_t s = (cudaStream_t)stream;
   WsHeader *hdr = static_cast<WsHeader *>(ws);
-  MOE_TRY_CUDA(cudaMemsetAsync(hdr, 0, sizeof(WsHeader), s));
+  // status word and (bf16) the per-tile split counters start at zero
+  MOE_TRY_CUDA(cudaMemsetAsync(hdr, 0, dtype == MOE_F32 ? sizeof(WsHeader) : kHdrBytes + fwd_count_bytes(T), s));
   if (T == 0) return MOE_OK;
   if (dtype == MOE_F32) {
     float *L = logits ? logits : reinterpret_cast<float *>(static_cast<char *>(ws) + kHdrBytes);
@@ -444,6 +613,9 @@ extern "C" int moe_router_fwd(const void *x, const void *w_router, int T, int d,
   if (p.stages > R_MAX_STAGES) p.stages = R_MAX_STAGES;
   p.num_kb = (d + RBK - 1) / RBK;
   p.num_tiles = (int)(t_pad_of(T) / RBM);
+  fwd_splits(T, d, &p.splits, &p.kb_split);
+  p.tile_count = reinterpret_cast<uint32_t *>(static_cast<char *>(ws) + kHdrBytes);
+  p.partial = reinterpret_cast<float *>(static_cast<char *>(ws) + kHdrBytes + fwd_count_bytes(T));
   p.logits = logits;
   p.topk_idx = topk_idx;
   p.topk_w = topk_w;

@@ -1,7 +1,7 @@
 """Host-buffer pipeline: layer passes fed from, and returned to, pinned host memory.
 
-Each step copies the pass's inputs (x, logits, and grad_out for a training pass) from host to
-device, runs the layer through the C ABI, and copies the per-token results (out, and dx, d_logits
+Each step copies the pass's inputs (x, logits -- or none on a router layer, which computes them
+from x --, and grad_out for a training pass) from host to device, runs the layer through the C ABI, and copies the per-token results (out, and dx, d_logits
 for a training pass) back to host memory. The copies run on two streams of their own and overlap
 the neighbouring steps' compute: step i+1's inputs are uploaded while step i computes, and step
 i's results are downloaded while step i+1 computes. Device inputs and the layer's result tensors
@@ -46,7 +46,9 @@ class HostPipeline:
         self.inputs = []
         self.results = []
         for _ in range(depth):
-            inp = dict(x=torch.empty((T, d), **act), logits=torch.empty((T, E), **f32))
+            inp = dict(x=torch.empty((T, d), **act))
+            if not layer.router:
+                inp["logits"] = torch.empty((T, E), **f32)
             res = dict(out=torch.empty((T, d), **act))
             if self.backward:
                 inp["g"] = torch.empty((T, d), **act)
@@ -85,14 +87,15 @@ class HostPipeline:
         self.in_ready[s].record(self.h2d)
         self.pending.append(s)
 
-    def run(self, w_gate_up, w_down):
-        """Compute the oldest uploaded step and enqueue the download of its results."""
+    def run(self, w_gate_up, w_down, w_router=None):
+        """Compute the oldest uploaded step and enqueue the download of its results (w_router: the
+        router weights of a router layer)."""
         s = self.pending.pop(0)
         inp, res, lay = self.inputs[s], self.results[s], self.layer
         self.compute.wait_event(self.in_ready[s])
         self.compute.wait_event(self.res_free[s])
         lay.out = res["out"]
-        lay.forward(inp["x"], inp["logits"], w_gate_up, w_down, self.compute)
+        lay.forward(inp["x"], inp.get("logits"), w_gate_up, w_down, self.compute, w_router=w_router)
         if self.backward:
             lay.dx, lay.d_logits = res["dx"], res["d_logits"]
             lay.backward(inp["g"], w_gate_up, w_down, self.compute)
@@ -109,14 +112,14 @@ class HostPipeline:
         self.n_run += 1
         return StepResult(self.host_out[s], ev)
 
-    def submit(self, batch, w_gate_up, w_down, next_batch=None):
+    def submit(self, batch, w_gate_up, w_down, next_batch=None, w_router=None):
         """One step: upload `batch` unless it is already uploaded, enqueue the upload of `next_batch`
         (if given) so that it overlaps this step's compute, then run this step."""
         if not self.pending:
             self.upload(batch)
         if next_batch is not None:
             self.upload(next_batch)
-        return self.run(w_gate_up, w_down)
+        return self.run(w_gate_up, w_down, w_router)
 
     def join(self, stream=None):
         """Make `stream` (default: the compute stream) wait for every enqueued copy."""

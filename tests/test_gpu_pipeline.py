@@ -9,43 +9,46 @@ import moe_inputs
 pytestmark = pytest.mark.gpu
 
 
-@pytest.mark.parametrize("backward", [True, False], ids=["fwdbwd", "fwd"])
-def test_pipeline_matches_layer(backward):
+@pytest.mark.parametrize("backward,router", [(True, False), (False, False), (True, True)],
+                         ids=["fwdbwd", "fwd", "fwdbwd_router"])
+def test_pipeline_matches_layer(backward, router):
     from mixture_experts_layer_histogram_gb300 import HostPipeline, MoELayer
     w = moe_inputs.small("pipe", T=1000, d=256, E=8, k=2, f=256)
     wts = moe_inputs.make_all(w, "cuda")
     wgu, wd = wts["w_gate_up"], wts["w_down"]
+    wr = (moe_inputs.make_router_weight(w).float() * 3.0).to(w.torch_dtype).cuda() if router else None
     batches = []
     for i in range(5):
         gen = torch.Generator().manual_seed(100 + i)
-        b = dict(x=torch.randn(w.T, w.d, generator=gen).to(w.torch_dtype),
-                 logits=torch.randn(w.T, w.E, generator=gen))
+        b = dict(x=torch.randn(w.T, w.d, generator=gen).to(w.torch_dtype))
+        if not router:
+            b["logits"] = torch.randn(w.T, w.E, generator=gen)
         if backward:
             b["g"] = torch.randn(w.T, w.d, generator=gen).to(w.torch_dtype)
         batches.append({k: v.pin_memory() for k, v in b.items()})
-    ref = MoELayer(w.T, w.d, w.E, w.k, w.f, w.torch_dtype, "cuda", backward=backward)
+    ref = MoELayer(w.T, w.d, w.E, w.k, w.f, w.torch_dtype, "cuda", backward=backward, router=router)
     expect = []
     for b in batches:
         d = {k: v.cuda() for k, v in b.items()}
-        ref.forward(d["x"], d["logits"], wgu, wd)
+        ref.forward(d["x"], d.get("logits"), wgu, wd, w_router=wr)
         r = dict(out=ref.out.cpu())
         if backward:
             ref.backward(d["g"], wgu, wd)
-            r.update(dx=ref.dx.cpu(), d_logits=ref.d_logits.cpu())
+            r.update(dx=ref.dx.cpu(), d_logits=ref.d_logits.cpu())   # dx includes the router's share
         expect.append(r)
-    lay = MoELayer(w.T, w.d, w.E, w.k, w.f, w.torch_dtype, "cuda", backward=backward)
+    lay = MoELayer(w.T, w.d, w.E, w.k, w.f, w.torch_dtype, "cuda", backward=backward, router=router)
     pipe = HostPipeline(lay)
     assert pipe.h2d_bytes() == sum(v.numel() * v.element_size() for v in batches[0].values())
     got, prev = [], None
     for i, b in enumerate(batches):
-        step = pipe.submit(b, wgu, wd, next_batch=batches[i + 1] if i + 1 < len(batches) else None)
+        step = pipe.submit(b, wgu, wd, next_batch=batches[i + 1] if i + 1 < len(batches) else None, w_router=wr)
         if prev is not None:                        # step i-1's download overlaps step i's compute
             got.append({k: v.clone() for k, v in prev.wait().items()})
         prev = step
     got.append({k: v.clone() for k, v in prev.wait().items()})
     pipe.join()
     torch.cuda.synchronize()
-    assert lay.status() == (0, 0)
+    assert not any(lay.status())
     for i, (e, g) in enumerate(zip(expect, got)):
         assert set(e) == set(g)
         for k in e:
