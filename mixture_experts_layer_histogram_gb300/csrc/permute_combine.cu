@@ -10,7 +10,7 @@
 namespace moe {
 
 constexpr int kRowThreads = 256;   // 8 warps, one token per warp per iteration
-constexpr int kUnroll = 4;         // 16-byte vectors in flight per lane
+constexpr int kUnroll = 8;         // 16-byte vectors in flight per lane (a 4 KB row in one round trip)
 
 template <typename T> struct Elem;
 template <> struct Elem<float> {
@@ -85,7 +85,10 @@ __global__ void __launch_bounds__(kRowThreads) permute_kernel(const uint4 *__res
 }
 
 // ---------------------------------------------------------------------------------------------
-template <typename T, bool WEIGHTED>
+// KMAX: compile-time upper bound on k. Per 512-byte chunk of the output row every lane first issues
+// the loads of all k expert rows, then accumulates them in slot order (fp32), so a warp waits for
+// one memory latency per chunk rather than one per slot.
+template <typename T, bool WEIGHTED, int KMAX>
 __global__ void __launch_bounds__(kRowThreads) combine_kernel(const uint4 *__restrict__ y, const float *__restrict__ w,
                                                               const int32_t *__restrict__ row_of_slot, int64_t Tn,
                                                               int64_t row_vecs, int k, int64_t rows_max,
@@ -96,21 +99,31 @@ __global__ void __launch_bounds__(kRowThreads) combine_kernel(const uint4 *__res
   for (int64_t t = (int64_t)blockIdx.x * (kRowThreads / 32) + (threadIdx.x >> 5); t < Tn; t += nw) {
     const int myrow = load_row(row_of_slot, t, k, lane, rows_max);
     const float myw = (WEIGHTED && lane < k) ? __ldg(w + t * k + lane) : 1.0f;
-    // warp-uniform loop: every lane reaches every shuffle; loads and stores are predicated
+    int rows[KMAX];
+    float ws[KMAX];
+#pragma unroll
+    for (int j = 0; j < KMAX; ++j) {
+      rows[j] = j < k ? __shfl_sync(0xffffffffu, myrow, j) : -1;
+      ws[j] = j < k ? __shfl_sync(0xffffffffu, myw, j) : 0.0f;
+    }
+    // warp-uniform loop: loads and stores are predicated per lane
     for (int64_t v0 = 0; v0 < row_vecs; v0 += 32) {
       const int64_t v = v0 + lane;
       const bool act = v < row_vecs;
+      uint4 q[KMAX];
+#pragma unroll
+      for (int j = 0; j < KMAX; ++j)
+        if (rows[j] >= 0 && act) q[j] = ld_stream(y + (int64_t)rows[j] * row_vecs + v);
       float acc[N];
 #pragma unroll
       for (int i = 0; i < N; ++i) acc[i] = 0.0f;
-      for (int j = 0; j < k; ++j) {
-        int r = __shfl_sync(0xffffffffu, myrow, j);
-        float wj = __shfl_sync(0xffffffffu, myw, j);
-        if (r < 0 || !act) continue;
-        float val[N];
-        Elem<T>::unpack(ld_stream(y + (int64_t)r * row_vecs + v), val);
 #pragma unroll
-        for (int i = 0; i < N; ++i) acc[i] = WEIGHTED ? fmaf(wj, val[i], acc[i]) : acc[i] + val[i];
+      for (int j = 0; j < KMAX; ++j) {
+        if (rows[j] < 0 || !act) continue;
+        float val[N];
+        Elem<T>::unpack(q[j], val);
+#pragma unroll
+        for (int i = 0; i < N; ++i) acc[i] = WEIGHTED ? fmaf(ws[j], val[i], acc[i]) : acc[i] + val[i];
       }
       if (act) out[t * row_vecs + v] = Elem<T>::pack(acc);
     }
@@ -246,13 +259,23 @@ extern "C" int moe_combine_fwd(const void *y_perm, const float *topk_w, const in
   cudaStream_t s = (cudaStream_t)stream;
   const uint4 *y = (const uint4 *)y_perm;
   uint4 *o = (uint4 *)out;
+#define MOE_COMBINE(TYPE, W, KM) combine_kernel<TYPE, W, KM><<<nb, kRowThreads, 0, s>>>(y, topk_w, row_of_slot, T, rv, k, rows_max, o)
+#define MOE_COMBINE_K(TYPE, W)                     \
+  do {                                             \
+    if (k <= 2) MOE_COMBINE(TYPE, W, 2);           \
+    else if (k <= 4) MOE_COMBINE(TYPE, W, 4);      \
+    else if (k <= 8) MOE_COMBINE(TYPE, W, 8);      \
+    else MOE_COMBINE(TYPE, W, 16);                 \
+  } while (0)
   if (dtype == MOE_BF16) {
-    if (topk_w) combine_kernel<__nv_bfloat16, true><<<nb, kRowThreads, 0, s>>>(y, topk_w, row_of_slot, T, rv, k, rows_max, o);
-    else combine_kernel<__nv_bfloat16, false><<<nb, kRowThreads, 0, s>>>(y, topk_w, row_of_slot, T, rv, k, rows_max, o);
+    if (topk_w) MOE_COMBINE_K(__nv_bfloat16, true);
+    else MOE_COMBINE_K(__nv_bfloat16, false);
   } else {
-    if (topk_w) combine_kernel<float, true><<<nb, kRowThreads, 0, s>>>(y, topk_w, row_of_slot, T, rv, k, rows_max, o);
-    else combine_kernel<float, false><<<nb, kRowThreads, 0, s>>>(y, topk_w, row_of_slot, T, rv, k, rows_max, o);
+    if (topk_w) MOE_COMBINE_K(float, true);
+    else MOE_COMBINE_K(float, false);
   }
+#undef MOE_COMBINE_K
+#undef MOE_COMBINE
   MOE_CHECK_LAUNCH();
   return MOE_OK;
 }
