@@ -52,6 +52,24 @@ def _dist():
     return ws, rank, local
 
 
+# Replicas (one per GPU, no data-path collective): the job's time is the slowest rank's, and the
+# job processes world x T tokens per step. These helpers take any torch.distributed backend.
+def max_over_ranks(ms, world, device):
+    """The largest of every rank's `ms` (the value itself when alone)."""
+    if world == 1:
+        return ms
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([ms], device=device, dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tokens_per_s(world, tokens_per_rank, steps, ms):
+    """Whole-job throughput: every rank's tokens over the max-over-ranks time of `steps` steps."""
+    return world * tokens_per_rank * steps / (ms * 1e-3)
+
+
 class ClockSampler:
     """nvidia-smi clock / throttle-reason samples, kept only if taken inside the timed window."""
 
@@ -205,11 +223,7 @@ def run_ours(args):
     clk.stop()
     if world > 1:
         dist.barrier()
-    elapsed_ms = t_start.elapsed_time(t_end)
-    if world > 1:
-        tt = torch.tensor([elapsed_ms], device=dev, dtype=torch.float64)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        elapsed_ms = float(tt.item())
+    elapsed_ms = max_over_ranks(t_start.elapsed_time(t_end), world, dev)
     per = {n: statistics.mean(evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(args.steps))
            for j, n in enumerate(names)}
     st = layer.status()
@@ -240,11 +254,7 @@ def run_ours(args):
     pipe.join()
     e1.record(stream)
     torch.cuda.synchronize(dev)
-    e2e_ms = e0.elapsed_time(e1)
-    if world > 1:
-        tt = torch.tensor([e2e_ms], device=dev, dtype=torch.float64)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        e2e_ms = float(tt.item())
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), world, dev)
     st = layer.status()
     if any(st):
         raise RuntimeError(f"device status after the end-to-end run: {st}")
@@ -283,7 +293,7 @@ def run_ours(args):
     kern["grouped_ffn_fwd"]["TFLOPs"] = round(6.0 * M * w.d * w.f / (per["grouped_ffn_fwd"] * 1e-3) / 1e12, 1)
     if bwd:
         kern["grouped_ffn_bwd"]["TFLOPs"] = round(12.0 * M * w.d * w.f / (per["grouped_ffn_bwd"] * 1e-3) / 1e12, 1)
-    value = world * w.T * args.steps / (elapsed_ms * 1e-3)
+    value = job_tokens_per_s(world, w.T, args.steps, elapsed_ms)
     if w.dtype == "bf16":
         roofline = {"kernel": "grouped SwiGLU GEMM (tcgen05; per step: fwd GATEUP, DOWN" +
                               ("; bwd DH, WGRAD down, DGRAD, WGRAD gate/up)" if bwd else ")"),
@@ -308,7 +318,7 @@ def run_ours(args):
                    "l2": "inputs larger than L2 (expert weights 768 MiB, grouped activations > 129 MB); no flush"},
         "roofline": roofline,
         "kernels": kern,
-        "e2e": {"value": round(world * w.T * args.steps / (e2e_ms * 1e-3), 1), "unit": "tokens/s",
+        "e2e": {"value": round(job_tokens_per_s(world, w.T, args.steps, e2e_ms), 1), "unit": "tokens/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms / args.steps, 4),
                 "api": "HostPipeline.submit (pinned host inputs and results; copies overlap compute)"},
         "gpu_launches": layer.launches(bwd) * args.steps,
