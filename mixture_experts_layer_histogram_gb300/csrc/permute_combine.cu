@@ -11,6 +11,7 @@ namespace moe {
 
 constexpr int kRowThreads = 256;   // 8 warps, one token per warp per iteration
 constexpr int kUnroll = 8;         // 16-byte vectors in flight per lane (a 4 KB row in one round trip)
+constexpr int kSegVecs = 128;      // combine: 16-byte vectors of a row per work unit (2 KB)
 
 template <typename T> struct Elem;
 template <> struct Elem<float> {
@@ -96,7 +97,12 @@ __global__ void __launch_bounds__(kRowThreads) combine_kernel(const uint4 *__res
   constexpr int N = Elem<T>::N;
   const int lane = threadIdx.x & 31;
   const int64_t nw = (int64_t)gridDim.x * (kRowThreads / 32);
-  for (int64_t t = (int64_t)blockIdx.x * (kRowThreads / 32) + (threadIdx.x >> 5); t < Tn; t += nw) {
+  // work unit: one kSegVecs-vector segment of one token's row (finer units balance the last wave)
+  const int64_t nseg = (row_vecs + kSegVecs - 1) / kSegVecs;
+  for (int64_t u = (int64_t)blockIdx.x * (kRowThreads / 32) + (threadIdx.x >> 5); u < Tn * nseg; u += nw) {
+    const int64_t t = u / nseg;
+    const int64_t vbeg = (u - t * nseg) * kSegVecs;
+    const int64_t vend = vbeg + kSegVecs < row_vecs ? vbeg + kSegVecs : row_vecs;
     const int myrow = load_row(row_of_slot, t, k, lane, rows_max);
     const float myw = (WEIGHTED && lane < k) ? __ldg(w + t * k + lane) : 1.0f;
     int rows[KMAX];
@@ -107,9 +113,9 @@ __global__ void __launch_bounds__(kRowThreads) combine_kernel(const uint4 *__res
       ws[j] = j < k ? __shfl_sync(0xffffffffu, myw, j) : 0.0f;
     }
     // warp-uniform loop: loads and stores are predicated per lane
-    for (int64_t v0 = 0; v0 < row_vecs; v0 += 32) {
+    for (int64_t v0 = vbeg; v0 < vend; v0 += 32) {
       const int64_t v = v0 + lane;
-      const bool act = v < row_vecs;
+      const bool act = v < vend;
       uint4 q[KMAX];
 #pragma unroll
       for (int j = 0; j < KMAX; ++j)
@@ -255,7 +261,7 @@ extern "C" int moe_combine_fwd(const void *y_perm, const float *topk_w, const in
   if (T == 0) return MOE_OK;
   if (!y_perm || !row_of_slot || !out || !aligned16(y_perm) || !aligned16(out)) return MOE_ERR_INVALID_ARG;
   const int64_t rv = (int64_t)(row_bytes / 16);
-  const int nb = row_blocks(T);
+  const int nb = row_blocks((int64_t)T * ((rv + kSegVecs - 1) / kSegVecs));   // one warp per row segment
   cudaStream_t s = (cudaStream_t)stream;
   const uint4 *y = (const uint4 *)y_perm;
   uint4 *o = (uint4 *)out;
