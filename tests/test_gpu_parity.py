@@ -48,6 +48,8 @@ SMALL = [
     moe_inputs.small("bf16_uniform", T=512, d=256, E=16, k=4, f=512, routing="uniform"),
     moe_inputs.small("bf16_single_expert", T=300, d=256, E=1, k=1, f=256),
     moe_inputs.small("f32_ragged", T=333, d=96, E=5, k=3, f=40, dtype="f32"),
+    moe_inputs.small("bf16_max_experts_topk", T=512, d=256, E=256, k=16, f=256),    # E and k at the ABI maximum
+    moe_inputs.small("f32_topk16", T=100, d=32, E=32, k=16, f=24, dtype="f32"),
 ]
 
 
