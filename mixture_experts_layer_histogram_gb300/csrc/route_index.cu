@@ -9,11 +9,13 @@
 //                  finds, per expert, how many earlier slots went to that expert with a decoupled
 //                  look-back over the preceding blocks (one 64-bit flag|value word per block and
 //                  expert), and scatters row_of_slot / token_of_row.
+#include <math.h>
+
 #include "common.cuh"
 
 namespace moe {
 
-constexpr int kRouteThreads = 256;
+constexpr int kRouteThreads = 128;               // tokens (threads) per routing block
 constexpr int kIdxThreads = 256;                 // 8 warps
 constexpr int kIdxItems = 4;                     // slots per thread
 constexpr int kIdxChunk = kIdxThreads * kIdxItems;
@@ -23,52 +25,58 @@ constexpr uint64_t kFlagAggregate = 1ull << 32;
 constexpr uint64_t kFlagPrefix = 2ull << 32;
 
 // ---------------------------------------------------------------------------------------------
-// top-k routing: one warp per token; lane l owns experts l, l+32, ...
-template <int EPL>
+// top-k routing: one thread per token. The thread reads its row of logits 64 at a time (16 vector
+// loads issued before any is used, so one memory latency per 64 experts), walks it in increasing
+// expert id inserting into a sorted top-k list held in registers (value desc, id asc: an equal
+// value never displaces a lower id; -0 == +0), then takes the softmax of the selected logits.
+template <int KMAX>
 __global__ void __launch_bounds__(kRouteThreads) route_topk_kernel(const float *__restrict__ logits, int T, int E,
                                                                    int k, int32_t *__restrict__ topk_idx,
                                                                    float *__restrict__ topk_w) {
-  const int lane = threadIdx.x & 31;
-  const int nwarps = gridDim.x * (kRouteThreads / 32);
-  for (int t = blockIdx.x * (kRouteThreads / 32) + (threadIdx.x >> 5); t < T; t += nwarps) {
-    float v[EPL];
+  const int64_t t = (int64_t)blockIdx.x * kRouteThreads + threadIdx.x;
+  if (t >= T) return;
+  const float *row = logits + t * E;
+  const bool vec = (E & 3) == 0;   // rows then start on 16-byte boundaries
+  float tv[KMAX];
+  int ti[KMAX];
 #pragma unroll
-    for (int i = 0; i < EPL; ++i) {
-      int e = lane + 32 * i;
-      v[i] = e < E ? __ldg(logits + (size_t)t * E + e) : 0.0f;
-    }
-    uint32_t taken = 0;
-    int my_e = 0;
-    float my_v = 0.0f;
-    for (int j = 0; j < k; ++j) {
-      float bv = 0.0f;
-      int be = 0x7fffffff;   // "no candidate"
-#pragma unroll
-      for (int i = 0; i < EPL; ++i) {
-        int e = lane + 32 * i;
-        bool ok = e < E && !((taken >> i) & 1u);
-        if (ok && (be == 0x7fffffff || v[i] > bv)) { bv = v[i]; be = e; }   // ascending e: ties keep lower id
-      }
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) {
-        float ov = __shfl_xor_sync(0xffffffffu, bv, off);
-        int oe = __shfl_xor_sync(0xffffffffu, be, off);
-        bool take = (oe != 0x7fffffff) && (be == 0x7fffffff || ov > bv || (ov == bv && oe < be));
-        if (take) { bv = ov; be = oe; }
-      }
-      if ((be & 31) == lane) taken |= 1u << (be >> 5);
-      if (lane == j) { my_e = be; my_v = bv; }
-    }
-    const float m = __shfl_sync(0xffffffffu, my_v, 0);   // largest selected logit
-    float ex = lane < k ? expf(my_v - m) : 0.0f;
-    float s = ex;
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
-    if (lane < k) {
-      topk_idx[(size_t)t * k + lane] = my_e;
-      topk_w[(size_t)t * k + lane] = ex / s;
-    }
+  for (int j = 0; j < KMAX; ++j) {
+    tv[j] = -INFINITY;
+    ti[j] = 0;
   }
+  for (int e0 = 0; e0 < E; e0 += 64) {
+    float v[64];
+    if (vec) {
+#pragma unroll
+      for (int q = 0; q < 16; ++q) {
+        const float4 f = e0 + 4 * q < E ? __ldg(reinterpret_cast<const float4 *>(row + e0) + q)
+                                        : make_float4(0.f, 0.f, 0.f, 0.f);
+        v[4 * q] = f.x;
+        v[4 * q + 1] = f.y;
+        v[4 * q + 2] = f.z;
+        v[4 * q + 3] = f.w;
+      }
+    } else {
+#pragma unroll
+      for (int i = 0; i < 64; ++i) v[i] = e0 + i < E ? __ldg(row + e0 + i) : 0.0f;
+    }
+#pragma unroll
+    for (int i = 0; i < 64; ++i)
+      if (e0 + i < E) topk_insert<KMAX>(tv, ti, v[i], e0 + i);
+  }
+  const float m = tv[0];
+  float ex[KMAX], s = 0.0f;
+#pragma unroll
+  for (int j = 0; j < KMAX; ++j) {
+    ex[j] = j < k ? expf(tv[j] - m) : 0.0f;
+    s += ex[j];
+  }
+#pragma unroll
+  for (int j = 0; j < KMAX; ++j)
+    if (j < k) {
+      topk_idx[t * k + j] = ti[j];
+      topk_w[t * k + j] = ex[j] / s;
+    }
 }
 
 // ---------------------------------------------------------------------------------------------
@@ -268,15 +276,14 @@ extern "C" int moe_route_topk(const float *logits, int T, int E, int k, int32_t 
   if (T < 0 || E < 1 || E > MOE_MAX_EXPERTS || k < 1 || k > E || k > MOE_MAX_TOPK) return MOE_ERR_INVALID_ARG;
   if (T == 0) return MOE_OK;
   if (!logits || !topk_idx || !topk_w) return MOE_ERR_INVALID_ARG;
-  const int warps = kRouteThreads / 32;
-  int blocks = (int)(((int64_t)T + warps - 1) / warps);
-  const int cap = sm_count() * 16;
-  if (blocks > cap) blocks = cap;
+  const int blocks = (int)(((int64_t)T + kRouteThreads - 1) / kRouteThreads);
   cudaStream_t s = (cudaStream_t)stream;
-  if (E <= 32) route_topk_kernel<1><<<blocks, kRouteThreads, 0, s>>>(logits, T, E, k, topk_idx, topk_w);
-  else if (E <= 64) route_topk_kernel<2><<<blocks, kRouteThreads, 0, s>>>(logits, T, E, k, topk_idx, topk_w);
-  else if (E <= 128) route_topk_kernel<4><<<blocks, kRouteThreads, 0, s>>>(logits, T, E, k, topk_idx, topk_w);
-  else route_topk_kernel<8><<<blocks, kRouteThreads, 0, s>>>(logits, T, E, k, topk_idx, topk_w);
+#define MOE_ROUTE(KM) route_topk_kernel<KM><<<blocks, kRouteThreads, 0, s>>>(logits, T, E, k, topk_idx, topk_w)
+  if (k <= 2) MOE_ROUTE(2);
+  else if (k <= 4) MOE_ROUTE(4);
+  else if (k <= 8) MOE_ROUTE(8);
+  else MOE_ROUTE(16);
+#undef MOE_ROUTE
   MOE_CHECK_LAUNCH();
   return MOE_OK;
 }

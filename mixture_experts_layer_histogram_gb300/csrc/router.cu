@@ -71,25 +71,6 @@ struct FwdParams {
   float *topk_w;
 };
 
-// Insert (v, e) into the list tv/ti (sorted by value desc, then id asc). Ids arrive in increasing
-// order, so v goes after every entry >= v, the entries after it shift down one place and the last
-// one drops out. Every slot's new content is computed from the old list at once (one comparison
-// per slot), which keeps the dependent chain per insertion short.
-template <int KMAX>
-__device__ __forceinline__ void topk_insert(float (&tv)[KMAX], int (&ti)[KMAX], float v, int e) {
-  bool ge[KMAX];
-#pragma unroll
-  for (int j = 0; j < KMAX; ++j) ge[j] = tv[j] >= v;
-#pragma unroll
-  for (int j = KMAX - 1; j >= 0; --j) {
-    const bool prev_ge = j == 0 ? true : ge[j > 0 ? j - 1 : 0];
-    const float pv = j == 0 ? v : tv[j > 0 ? j - 1 : 0];
-    const int pi = j == 0 ? e : ti[j > 0 ? j - 1 : 0];
-    tv[j] = ge[j] ? tv[j] : (prev_ge ? v : pv);
-    ti[j] = ge[j] ? ti[j] : (prev_ge ? e : pi);
-  }
-}
-
 // True on every epilogue thread (the 256 threads of warps 2..9) if `v` holds on any of them.
 __device__ __forceinline__ bool epi_any(bool v) {
   uint32_t r;
