@@ -45,8 +45,6 @@ __device__ __forceinline__ void report(WsHeader *ws, int code, int detail) {
   if (atomicCAS(&ws->status, 0, code) == 0) ws->detail = detail;
 }
 
-__device__ __forceinline__ float bf16_to_f(uint16_t u) { return __uint_as_float((uint32_t)u << 16); }
-
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);   // round to nearest even
   return *reinterpret_cast<uint32_t *>(&v);

@@ -831,43 +831,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     for (int tile = cluster_id; tile < num_tiles; tile += num_clusters) {
       bool valid;
       const Tile t = decode_pair<KIND>(tile, p, toff, ptoff, (int)rank, valid);
-      if (t.kb == 0) {   // a group with no rows: its gradient (partial) is zero
-        if (KIND == RDW) {
-          const int er = t.m0 + row_in_tile;
-          if (er < p.rows_valid) {
-            float *dst = p.outf + ((int64_t)t.e * p.rows_valid + er) * p.ldf + t.n0 + c0;
-            for (int i = 0; i < BN / 2; i += 4)
-              if (t.n0 + c0 + i < p.d) *reinterpret_cast<float4 *>(dst + i) = make_float4(0.f, 0.f, 0.f, 0.f);
-          }
-        } else {
-          __nv_bfloat16 *dst =
-              p.out0 + (int64_t)t.e * p.out_e_stride + (int64_t)(t.m0 + row_in_tile) * p.ld0 + t.n0 + c0;
-          uint4 *q = reinterpret_cast<uint4 *>(dst);
-          for (int i = 0; i < BN / 16; ++i) q[i] = make_uint4(0, 0, 0, 0);
-        }
+      if (t.kb == 0) {   // WGRAD of an expert with no rows: the gradient is zero
+        __nv_bfloat16 *dst =
+            p.out0 + (int64_t)t.e * p.out_e_stride + (int64_t)(t.m0 + row_in_tile) * p.ld0 + t.n0 + c0;
+        uint4 *q = reinterpret_cast<uint4 *>(dst);
+        for (int i = 0; i < BN / 16; ++i) q[i] = make_uint4(0, 0, 0, 0);
         continue;
       }
-      uint4 pre[pre_count(KIND)];
-      if (KIND == DH) {   // the next tile's a, b rows of this thread: into L2 now, read one tile later
-        const int nxt = tile + num_clusters;
-        if (nxt < num_tiles) {
-          bool nvalid;
-          const Tile tn = decode_pair<KIND>(nxt, p, toff, ptoff, (int)rank, nvalid);
-          if (nvalid) {
-            const __nv_bfloat16 *nrow = p.aux + (int64_t)(tn.m0 + row_in_tile) * p.ld_aux + tn.n0 + c0;
-            l2_prefetch_bytes(nrow, (BN / 2) * 2);
-            l2_prefetch_bytes(nrow + p.f, (BN / 2) * 2);
-          }
-        }
-      }
-      if (KIND == DH && valid) {
-        const __nv_bfloat16 *abrow = p.aux + (int64_t)(t.m0 + row_in_tile) * p.ld_aux + t.n0 + c0;
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          pre[i] = reinterpret_cast<const uint4 *>(abrow)[i];
-          pre[4 + i] = reinterpret_cast<const uint4 *>(abrow + p.f)[i];
-        }
-      }
+      uint4 pre[pre_count(KIND)];   // unused here: the pair kernel's DH has its own epilogue above
       if (!mbar_wait_cluster(tfull_bar(acc), acc_phase, abort_flag, p.hdr, 14)) break;
       tc_fence_after();
       const uint32_t tbase = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * BN);
