@@ -198,9 +198,12 @@ def run_ours(args):
             L.moe_router_bwd(x, wr, layer.d_logits, layer.dx, layer.dw_router, layer.ws_router, accumulate_dx=True)
         ev[9].record(stream)
 
+    graph = None
+    if args.graph:   # the timed steps replay one captured pass; per-kernel times come from a separate eager pass
+        graph = layer.capture(x, None if args.router else logits, wgu, wd, grad_out=g if bwd else None, w_router=wr)
     clk = ClockSampler(dev.index).start()
     for _ in range(args.warmup):
-        step()
+        step() if graph is None else graph.replay()
     torch.cuda.synchronize(dev)
     st = layer.status()
     if any(st):
@@ -216,7 +219,7 @@ def run_ours(args):
     w0 = time.time()
     t_start.record(stream)
     for i in range(args.steps):
-        step(evs[i])
+        step(evs[i]) if graph is None else graph.replay()
     t_end.record(stream)
     torch.cuda.synchronize(dev)
     clk.window = (w0, time.time())
@@ -224,7 +227,12 @@ def run_ours(args):
     if world > 1:
         dist.barrier()
     elapsed_ms = max_over_ranks(t_start.elapsed_time(t_end), world, dev)
-    per = {n: statistics.mean(evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(args.steps))
+    if graph is not None:   # per-kernel times from an eager pass with events (not part of the timed steps)
+        for i in range(3):
+            step(evs[i])
+        torch.cuda.synchronize(dev)
+    nper = 3 if graph is not None else args.steps
+    per = {n: statistics.mean(evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(nper))
            for j, n in enumerate(names)}
     st = layer.status()
     if any(st):
@@ -314,7 +322,7 @@ def run_ours(args):
         "config": {"workload": w.name, "T": w.T, "d": w.d, "E": w.E, "k": w.k, "f": w.f, "routing": w.routing,
                    "pass": (("fwd+bwd (recompute)" if args.recompute else "fwd+bwd") if bwd else "fwd") +
                            (", router GEMM in the pass" if args.router else ""),
-                   "parallelism": f"replicas x{world}",
+                   "parallelism": f"replicas x{world}", "launch": "cuda graph" if args.graph else "eager",
                    "l2": "inputs larger than L2 (expert weights 768 MiB, grouped activations > 129 MB); no flush"},
         "roofline": roofline,
         "kernels": kern,
@@ -403,6 +411,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--router", action="store_true",
                     help="the pass starts from x and router weights: router GEMM with fused top-k, and its backward")
+    ap.add_argument("--graph", action="store_true",
+                    help="time the steps as replays of one CUDA graph of the pass (one host launch per step)")
     ap.add_argument("--recompute", action="store_true",
                     help="backward recomputes ab, h from x_perm (selective activation checkpointing)")
     ap.add_argument("--ref-tokens", type=int, default=8)

@@ -116,6 +116,26 @@ class MoELayer:
             res["dw_router"] = self.dw_router
         return res
 
+    def capture(self, x, logits, w_gate_up, w_down, grad_out=None, w_router=None):
+        """Record one pass (forward, and backward when grad_out is given) on these tensors into a
+        CUDA graph and return it; graph.replay() re-runs the whole pass on whatever the tensors hold
+        then, with one launch from the host instead of one per kernel. The call runs the pass
+        twice on a side stream first (the library's one-time set-up happens outside the capture)."""
+        def step():
+            self.forward(x, logits, w_gate_up, w_down, w_router=w_router)
+            if grad_out is not None:
+                self.backward(grad_out, w_gate_up, w_down)
+        side = torch.cuda.Stream(self.device)
+        side.wait_stream(torch.cuda.current_stream(self.device))
+        with torch.cuda.stream(side):
+            for _ in range(2):
+                step()
+        torch.cuda.current_stream(self.device).wait_stream(side)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            step()
+        return graph
+
     def status(self, stream=None):
         """Device status words (synchronises): (count_index, grouped_ffn), plus the router's on a router layer."""
         st = (L.moe_read_status(self.ws_index, stream), L.moe_read_status(self.ws_ffn, stream))
