@@ -39,7 +39,7 @@ def _rank_main(rank, world, port, out):
 def test_max_over_ranks_and_job_throughput_gloo():
     world = 2
     port = _free_port()
-    with mp.Manager() as m:
+    with mp.get_context("spawn").Manager() as m:   # spawn, never fork, from a process with threads
         out = m.dict()
         mp.spawn(_rank_main, args=(world, port, out), nprocs=world, join=True)
         res = dict(out)
