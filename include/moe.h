@@ -109,8 +109,8 @@ int moe_count_index(const int32_t *topk_idx, int T, int k, int E, int32_t *count
  * scratch lives in a fixed device array of MOE_STATIC_SCRATCH_BYTES inside the library, present on
  * every GPU that loads the library until the process exits.
  *   - Size limit: calls whose moe_count_index_workspace_size(T, k, E) exceeds
- *     MOE_STATIC_SCRATCH_BYTES return MOE_ERR_UNSUPPORTED (1 MiB covers, e.g., T*k = 1M slots at
- *     E = 64, or T*k = 262,144 slots at E = 256).
+ *     MOE_STATIC_SCRATCH_BYTES return MOE_ERR_UNSUPPORTED (1 MiB covers T*k up to 2,095,104 slots at
+ *     E = 64, or up to 523,264 slots at E = 256).
  *   - The first call on a device looks up the array's device address (cudaGetSymbolAddress) and
  *     caches it; make that first call before any stream capture on that device.
  *   - Every call on a device shares the one array: calls that overlap on the GPU (different streams
