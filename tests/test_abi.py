@@ -108,6 +108,10 @@ def test_invalid_arguments_are_rejected_on_the_host(L):
     assert L.moe_router_bwd(FAKE, FAKE, FAKE, 64, 256, 8, 1, 0, FAKE, NULL, FAKE, rws, NULL) == -1
     assert L.moe_router_bwd(FAKE, FAKE, FAKE, 64, 256, 8, 2, 0, FAKE, FAKE, FAKE, rws, NULL) == -1
     assert L.moe_read_status(NULL, NULL) == -1
+    # allocation-free count/index: the stated limits are exactly where the 1 MiB scratch runs out
+    for E, slots in ((64, 2095104), (256, 523264)):
+        assert L.moe_count_index_workspace_size(slots, 1, E) <= 1 << 20 < L.moe_count_index_workspace_size(slots + 1, 1, E)
+        assert L.moe_count_index_static(FAKE, slots + 1, 1, E, FAKE, FAKE, FAKE, FAKE, FAKE, NULL) == -2
 
 
 def test_empty_inputs_enqueue_nothing(L):
