@@ -102,6 +102,22 @@ int moe_count_index(const int32_t *topk_idx, int T, int k, int E, int32_t *count
                     size_t ws_bytes, moe_stream_t stream);
 
 /* ---------------------------------------------------------------------------------------------
+ * Routing, token counting and index generation in one launch (brief, section 核心方法: expert
+ * selection feeding the GPU kernels for token counting and index generation): the results of
+ * moe_route_topk followed by moe_count_index, bit for bit (topk_idx, topk_w, counts, offsets,
+ * tile_offsets, row_of_slot, token_of_row), from one kernel that routes a block's tokens, ranks
+ * its slots, publishes its counts and look-back aggregates, and scatters once the last block has
+ * scanned the totals. Arguments, shapes, workspace size and device errors are those of the two
+ * calls (the selection cannot produce an expert id outside [0, E)); the look-back fault hook is not
+ * read and is cleared. The blocks wait for one another, so the kernel runs only when all of them
+ * fit on the GPU at once (T*k up to about 300K slots on a GB300); above that the call makes the
+ * two separate calls itself.
+ */
+int moe_route_count_index(const float *logits, int T, int E, int k, int32_t *topk_idx, float *topk_w,
+                          int32_t *counts, int32_t *offsets, int32_t *tile_offsets, int32_t *row_of_slot,
+                          int32_t *token_of_row, void *ws, size_t ws_bytes, moe_stream_t stream);
+
+/* ---------------------------------------------------------------------------------------------
  * moe_count_index without a workspace. The paper has no counterpart: this entry point exists for
  * callers that cannot allocate device memory (for example a plugin inside a host framework that
  * owns all device allocations and passes only input and output buffers, or a service that forbids

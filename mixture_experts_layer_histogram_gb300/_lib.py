@@ -32,6 +32,7 @@ _SIGS = {
     "moe_count_index_hook_offset": (_SZ, [_I]),
     "moe_count_index": (_I, [_P, _I, _I, _I, _P, _P, _P, _P, _P, _P, _SZ, _P]),
     "moe_count_index_static": (_I, [_P, _I, _I, _I, _P, _P, _P, _P, _P, _P]),
+    "moe_route_count_index": (_I, [_P, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]),
     "moe_permute": (_I, [_P, _I, _I, _I, _I, _I, _P, _P, _P, _I64, _P, _P]),
     "moe_grouped_ffn_workspace_size": (_SZ, [_I, _I, _I, _I64, _I, _I]),
     "moe_grouped_ffn_fwd": (_I, [_P, _P, _P, _P, _I, _I, _I, _I64, _I, _P, _P, _P, _P, _SZ, _P]),
@@ -123,6 +124,15 @@ def moe_count_index(topk_idx, E, counts, offsets, tile_offsets, row_of_slot, tok
     _ok("moe_count_index", lib().moe_count_index(_p(topk_idx), T, k, E, _p(counts), _p(offsets), _p(tile_offsets),
                                                  _p(row_of_slot), _p(token_of_row), _p(ws), ws.numel() * ws.element_size(),
                                                  _s(stream)))
+
+
+def moe_route_count_index(logits, k, topk_idx, topk_w, counts, offsets, tile_offsets, row_of_slot, token_of_row, ws,
+                          stream=None):
+    """moe_route_topk then moe_count_index, in one launch when all its blocks fit on the GPU."""
+    T, E = logits.shape
+    _ok("moe_route_count_index", lib().moe_route_count_index(
+        _p(logits), T, E, k, _p(topk_idx), _p(topk_w), _p(counts), _p(offsets), _p(tile_offsets), _p(row_of_slot),
+        _p(token_of_row), _p(ws), ws.numel() * ws.element_size(), _s(stream)))
 
 
 def moe_count_index_static(topk_idx, E, counts, offsets, tile_offsets, row_of_slot, token_of_row, stream=None):

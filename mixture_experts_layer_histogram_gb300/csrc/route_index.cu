@@ -30,15 +30,11 @@ constexpr uint64_t kFlagPrefix = 2ull << 32;
 // expert id inserting into a sorted top-k list held in registers (value desc, id asc: an equal
 // value never displaces a lower id; -0 == +0), then takes the softmax of the selected logits.
 template <int KMAX>
-__global__ void __launch_bounds__(kRouteThreads) route_topk_kernel(const float *__restrict__ logits, int T, int E,
-                                                                   int k, int32_t *__restrict__ topk_idx,
-                                                                   float *__restrict__ topk_w) {
-  const int64_t t = (int64_t)blockIdx.x * kRouteThreads + threadIdx.x;
-  if (t >= T) return;
+__device__ __forceinline__ void route_token(const float *__restrict__ logits, int64_t t, int E, int k,
+                                            int (&ti)[KMAX], float (&w)[KMAX]) {
   const float *row = logits + t * E;
   const bool vec = (E & 3) == 0;   // rows then start on 16-byte boundaries
   float tv[KMAX];
-  int ti[KMAX];
 #pragma unroll
   for (int j = 0; j < KMAX; ++j) {
     tv[j] = -INFINITY;
@@ -65,17 +61,30 @@ __global__ void __launch_bounds__(kRouteThreads) route_topk_kernel(const float *
       if (e0 + i < E) topk_insert<KMAX>(tv, ti, v[i], e0 + i);
   }
   const float m = tv[0];
-  float ex[KMAX], s = 0.0f;
+  float s = 0.0f;
 #pragma unroll
   for (int j = 0; j < KMAX; ++j) {
-    ex[j] = j < k ? expf(tv[j] - m) : 0.0f;
-    s += ex[j];
+    w[j] = j < k ? expf(tv[j] - m) : 0.0f;
+    s += w[j];
   }
+#pragma unroll
+  for (int j = 0; j < KMAX; ++j) w[j] = w[j] / s;
+}
+
+template <int KMAX>
+__global__ void __launch_bounds__(kRouteThreads) route_topk_kernel(const float *__restrict__ logits, int T, int E,
+                                                                   int k, int32_t *__restrict__ topk_idx,
+                                                                   float *__restrict__ topk_w) {
+  const int64_t t = (int64_t)blockIdx.x * kRouteThreads + threadIdx.x;
+  if (t >= T) return;
+  int ti[KMAX];
+  float w[KMAX];
+  route_token<KMAX>(logits, t, E, k, ti, w);
 #pragma unroll
   for (int j = 0; j < KMAX; ++j)
     if (j < k) {
       topk_idx[t * k + j] = ti[j];
-      topk_w[t * k + j] = ex[j] / s;
+      topk_w[t * k + j] = w[j];
     }
 }
 
@@ -93,6 +102,44 @@ __device__ __forceinline__ int slot_key(const int32_t *__restrict__ idx, int64_t
     return -1;
   }
   return e;
+}
+
+// Exclusive scans of the per-expert totals in acc: counts, offsets (scan of counts) and tile_offsets
+// (scan of ceil(counts / BM)). One warp, 8 experts per lane (E <= 256).
+__device__ __forceinline__ void scan_counts(int32_t *acc, int E, int BM, int32_t *__restrict__ counts,
+                                            int32_t *__restrict__ offsets, int32_t *__restrict__ tile_offsets) {
+  const int lane = threadIdx.x & 31;
+  int c[8], tl[8], sc = 0, st = 0;
+#pragma unroll
+  for (int q = 0; q < 8; ++q) {
+    int e = lane * 8 + q;
+    c[q] = e < E ? atomicAdd(acc + e, 0) : 0;
+    tl[q] = (c[q] + BM - 1) / BM;
+    sc += c[q];
+    st += tl[q];
+  }
+  int ic = sc, it = st;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    int a = __shfl_up_sync(0xffffffffu, ic, off), b = __shfl_up_sync(0xffffffffu, it, off);
+    if (lane >= off) { ic += a; it += b; }
+  }
+  int rc = ic - sc, rt = it - st;   // exclusive prefix of this lane's first expert
+#pragma unroll
+  for (int q = 0; q < 8; ++q) {
+    int e = lane * 8 + q;
+    if (e < E) {
+      counts[e] = c[q];
+      offsets[e] = rc;
+      tile_offsets[e] = rt;
+    }
+    rc += c[q];
+    rt += tl[q];
+  }
+  if (lane == 31) {
+    offsets[E] = ic;
+    tile_offsets[E] = it;
+  }
 }
 
 __global__ void __launch_bounds__(kIdxThreads) count_kernel(const int32_t *__restrict__ idx, int64_t n, int E, int BM,
@@ -128,70 +175,20 @@ __global__ void __launch_bounds__(kIdxThreads) count_kernel(const int32_t *__res
     hdr->armed = *hook;
     *hook = 0;
   }
-  // last block: exclusive scans of counts and of ceil(counts / BM); warp 0, 8 experts per lane
-  if (tid < 32) {
-    int c[8], tl[8], sc = 0, st = 0;
-#pragma unroll
-    for (int q = 0; q < 8; ++q) {
-      int e = lane * 8 + q;
-      c[q] = e < E ? atomicAdd(acc + e, 0) : 0;
-      tl[q] = (c[q] + BM - 1) / BM;
-      sc += c[q];
-      st += tl[q];
-    }
-    int ic = sc, it = st;
-#pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-      int a = __shfl_up_sync(0xffffffffu, ic, off), b = __shfl_up_sync(0xffffffffu, it, off);
-      if (lane >= off) { ic += a; it += b; }
-    }
-    int rc = ic - sc, rt = it - st;   // exclusive prefix of this lane's first expert
-#pragma unroll
-    for (int q = 0; q < 8; ++q) {
-      int e = lane * 8 + q;
-      if (e < E) {
-        counts[e] = c[q];
-        offsets[e] = rc;
-        tile_offsets[e] = rt;
-      }
-      rc += c[q];
-      rt += tl[q];
-    }
-    if (lane == 31) {
-      offsets[E] = ic;
-      tile_offsets[E] = it;
-    }
-  }
+  if (tid < 32) scan_counts(acc, E, BM, counts, offsets, tile_offsets);
 }
 
 // ---------------------------------------------------------------------------------------------
-// index kernel: stable ranks + per-expert decoupled look-back + scatter
-__global__ void __launch_bounds__(kIdxThreads) index_kernel(const int32_t *__restrict__ idx, int64_t n, int k, int E,
-                                                            int BM, WsHeader *hdr, uint64_t *__restrict__ lookback,
-                                                            const int32_t *__restrict__ counts,
-                                                            const int32_t *__restrict__ tile_offsets,
-                                                            int32_t *__restrict__ row_of_slot,
-                                                            int32_t *__restrict__ token_of_row) {
-  __shared__ int warp_cnt[kIdxThreads / 32][MOE_MAX_EXPERTS];
-  __shared__ int run[MOE_MAX_EXPERTS];
-  __shared__ int excl[MOE_MAX_EXPERTS];
-  __shared__ int row_base[MOE_MAX_EXPERTS];
-  __shared__ int bid_s;
+// Stable ranks of a block's slots within their expert and the block's per-expert totals. key[i]
+// is the expert of the block's slot i * kIdxThreads + tid (-1: none). On return rank[i] counts the
+// block's earlier slots (in slot order) with the same expert and run[e] holds the block's count of
+// expert e. warp_cnt must be all zero on entry and is all zero again on return.
+__device__ __forceinline__ void block_ranks(const int (&key)[kIdxItems], int (&rank)[kIdxItems],
+                                            int (*warp_cnt)[MOE_MAX_EXPERTS], int *run, int E) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  if (tid == 0) bid_s = (int)atomicAdd(&hdr->tickets[1], 1u);   // dynamic block id: predecessors already run
-  for (int i = tid; i < (kIdxThreads / 32) * MOE_MAX_EXPERTS; i += kIdxThreads) (&warp_cnt[0][0])[i] = 0;
-  for (int e = tid; e < E; e += kIdxThreads) {
-    run[e] = 0;
-    row_base[e] = tile_offsets[e] * BM;
-  }
-  __syncthreads();
-  const int b = bid_s;
-  const int64_t base = (int64_t)b * kIdxChunk;
   const unsigned lt_mask = (1u << lane) - 1u;
-  int key[kIdxItems], rank[kIdxItems];
 #pragma unroll
   for (int i = 0; i < kIdxItems; ++i) {
-    key[i] = slot_key(idx, base + i * kIdxThreads + tid, n, E, nullptr);
     unsigned peers = __match_any_sync(0xffffffffu, key[i]);
     int r_in_warp = __popc(peers & lt_mask);
     bool leader = key[i] >= 0 && lane == __ffs(peers) - 1;
@@ -213,9 +210,16 @@ __global__ void __launch_bounds__(kIdxThreads) index_kernel(const int32_t *__res
     for (int j = tid; j < (kIdxThreads / 32) * MOE_MAX_EXPERTS; j += kIdxThreads) (&warp_cnt[0][0])[j] = 0;
     __syncthreads();
   }
-  // publish this block's per-expert aggregate, then look back over predecessors
-  const bool withhold = (b == hdr->armed - 1);
-  for (int e = tid; e < E; e += kIdxThreads) {
+}
+
+// Decoupled look-back: publish block b's per-expert aggregate run[e], walk back over the preceding
+// blocks' words (an aggregate adds and continues, an inclusive prefix adds and stops, a word not
+// yet published is waited for, at most about 0.2 s), set excl[e] to the number of slots of expert
+// e in blocks 0..b-1 and publish block b's inclusive prefix. `withhold` leaves this block's words
+// unpublished (the fault hook of moe_count_index).
+__device__ __forceinline__ void block_lookback(int b, int E, const int *run, int *excl, uint64_t *lookback,
+                                               WsHeader *hdr, bool withhold) {
+  for (int e = threadIdx.x; e < E; e += kIdxThreads) {
     const uint32_t agg = (uint32_t)run[e];
     volatile uint64_t *mine = lookback + (size_t)b * E + e;
     if (b == 0) {
@@ -247,6 +251,36 @@ __global__ void __launch_bounds__(kIdxThreads) index_kernel(const int32_t *__res
     excl[e] = (int)sum;
     if (!withhold) *mine = kFlagPrefix | (sum + agg);
   }
+}
+
+// ---------------------------------------------------------------------------------------------
+// index kernel: stable ranks + per-expert decoupled look-back + scatter
+__global__ void __launch_bounds__(kIdxThreads) index_kernel(const int32_t *__restrict__ idx, int64_t n, int k, int E,
+                                                            int BM, WsHeader *hdr, uint64_t *__restrict__ lookback,
+                                                            const int32_t *__restrict__ counts,
+                                                            const int32_t *__restrict__ tile_offsets,
+                                                            int32_t *__restrict__ row_of_slot,
+                                                            int32_t *__restrict__ token_of_row) {
+  __shared__ int warp_cnt[kIdxThreads / 32][MOE_MAX_EXPERTS];
+  __shared__ int run[MOE_MAX_EXPERTS];
+  __shared__ int excl[MOE_MAX_EXPERTS];
+  __shared__ int row_base[MOE_MAX_EXPERTS];
+  __shared__ int bid_s;
+  const int tid = threadIdx.x;
+  if (tid == 0) bid_s = (int)atomicAdd(&hdr->tickets[1], 1u);   // dynamic block id: predecessors already run
+  for (int i = tid; i < (kIdxThreads / 32) * MOE_MAX_EXPERTS; i += kIdxThreads) (&warp_cnt[0][0])[i] = 0;
+  for (int e = tid; e < E; e += kIdxThreads) {
+    run[e] = 0;
+    row_base[e] = tile_offsets[e] * BM;
+  }
+  __syncthreads();
+  const int b = bid_s;
+  const int64_t base = (int64_t)b * kIdxChunk;
+  int key[kIdxItems], rank[kIdxItems];
+#pragma unroll
+  for (int i = 0; i < kIdxItems; ++i) key[i] = slot_key(idx, base + i * kIdxThreads + tid, n, E, nullptr);
+  block_ranks(key, rank, warp_cnt, run, E);
+  block_lookback(b, E, run, excl, lookback, hdr, b == hdr->armed - 1);
   __syncthreads();
 #pragma unroll
   for (int i = 0; i < kIdxItems; ++i) {
@@ -263,6 +297,108 @@ __global__ void __launch_bounds__(kIdxThreads) index_kernel(const int32_t *__res
   // padding rows of the grouped layout
   for (int e = blockIdx.x; e < E; e += gridDim.x) {
     int start = tile_offsets[e] * BM + counts[e], end = tile_offsets[e + 1] * BM;
+    for (int r = start + tid; r < end; r += kIdxThreads) token_of_row[r] = -1;
+  }
+}
+
+// ---------------------------------------------------------------------------------------------
+// Routing, counting and index generation in one kernel (moe_route_count_index). Block b owns the
+// same kIdxChunk slots as index_kernel's block b. It routes the tokens those slots belong to (a
+// token whose slots straddle two blocks is routed by both, with identical results; the block
+// holding its first slot writes topk_idx / topk_w), ranks its slots stably per expert, adds its
+// counts to the global totals and publishes its look-back aggregate. The last block to do so
+// computes the scans (counts, offsets, tile_offsets) and raises a flag; meanwhile every block looks
+// back over its predecessors, then waits for the flag (bounded, about 0.2 s) and scatters. The
+// wait needs every block resident at once; the host launches this kernel only when they fit.
+template <int KMAX>
+__global__ void __launch_bounds__(kIdxThreads) route_count_index_kernel(
+    const float *__restrict__ logits, int T, int E, int k, int BM, WsHeader *hdr, int32_t *acc,
+    uint64_t *__restrict__ lookback, int32_t *__restrict__ topk_idx, float *__restrict__ topk_w, int32_t *counts,
+    int32_t *offsets, int32_t *tile_offsets, int32_t *__restrict__ row_of_slot, int32_t *__restrict__ token_of_row) {
+  __shared__ int sk[kIdxChunk];                       // experts of this block's slots, slot order
+  __shared__ int warp_cnt[kIdxThreads / 32][MOE_MAX_EXPERTS];
+  __shared__ int run[MOE_MAX_EXPERTS];
+  __shared__ int excl[MOE_MAX_EXPERTS];
+  __shared__ int row_base[MOE_MAX_EXPERTS];
+  __shared__ int bid_s;
+  __shared__ bool is_last, ready;
+  const int tid = threadIdx.x;
+  if (tid == 0) bid_s = (int)atomicAdd(&hdr->tickets[1], 1u);
+  for (int i = tid; i < (kIdxThreads / 32) * MOE_MAX_EXPERTS; i += kIdxThreads) (&warp_cnt[0][0])[i] = 0;
+  for (int e = tid; e < E; e += kIdxThreads) run[e] = 0;
+  __syncthreads();
+  const int b = bid_s;
+  const int64_t n = (int64_t)T * k;
+  const int64_t base = (int64_t)b * kIdxChunk;
+  const int64_t send = base + kIdxChunk < n ? base + kIdxChunk : n;   // this block's slots: [base, send)
+  // route the tokens of slots [base, send)
+  const int64_t t_first = base / k, t_last = (send - 1) / k;
+  for (int64_t t = t_first + tid; t <= t_last; t += kIdxThreads) {
+    int ti[KMAX];
+    float w[KMAX];
+    route_token<KMAX>(logits, t, E, k, ti, w);
+    const bool owner = t * k >= base;
+#pragma unroll
+    for (int j = 0; j < KMAX; ++j)
+      if (j < k) {
+        const int64_t s = t * k + j;
+        if (s >= base && s < send) sk[s - base] = ti[j];
+        if (owner) {
+          topk_idx[s] = ti[j];
+          topk_w[s] = w[j];
+        }
+      }
+  }
+  __syncthreads();
+  int key[kIdxItems], rank[kIdxItems];
+#pragma unroll
+  for (int i = 0; i < kIdxItems; ++i) {
+    const int64_t s = base + i * kIdxThreads + tid;
+    key[i] = s < send ? sk[s - base] : -1;
+  }
+  block_ranks(key, rank, warp_cnt, run, E);
+  for (int e = tid; e < E; e += kIdxThreads)
+    if (run[e]) atomicAdd(acc + e, run[e]);
+  __threadfence();
+  __syncthreads();
+  if (tid == 0) is_last = atomicAdd(&hdr->tickets[0], 1u) == gridDim.x - 1;
+  __syncthreads();
+  if (is_last) {
+    __threadfence();
+    if (tid < 32) scan_counts(acc, E, BM, counts, offsets, tile_offsets);
+    __threadfence();
+    __syncthreads();
+    if (tid == 0) atomicExch(&hdr->tickets[2], 1u);   // the scans are visible
+  }
+  block_lookback(b, E, run, excl, lookback, hdr, false);
+  if (tid == 0) {   // wait for the scans, bounded
+    bool ok = true;
+    const uint64_t t0 = global_ns();
+    while (atomicAdd(&hdr->tickets[2], 0u) == 0u) {
+      if (global_ns() - t0 > kWaitLimitNs) {
+        report(hdr, MOE_ERR_DEVICE_TIMEOUT, b);
+        ok = false;
+        break;
+      }
+      __nanosleep(128);
+    }
+    __threadfence();
+    ready = ok;
+  }
+  __syncthreads();
+  if (!ready) return;
+  for (int e = tid; e < E; e += kIdxThreads) row_base[e] = __ldcg(tile_offsets + e) * BM;
+  __syncthreads();
+#pragma unroll
+  for (int i = 0; i < kIdxItems; ++i) {
+    const int64_t s = base + i * kIdxThreads + tid;
+    if (s >= send) continue;
+    const int row = row_base[key[i]] + excl[key[i]] + rank[i];
+    row_of_slot[s] = row;
+    token_of_row[row] = (int)(s / k);
+  }
+  for (int e = blockIdx.x; e < E; e += gridDim.x) {   // padding rows of the grouped layout
+    const int start = __ldcg(tile_offsets + e) * BM + __ldcg(counts + e), end = __ldcg(tile_offsets + e + 1) * BM;
     for (int r = start + tid; r < end; r += kIdxThreads) token_of_row[r] = -1;
   }
 }
@@ -335,6 +471,64 @@ extern "C" int moe_count_index(const int32_t *topk_idx, int T, int k, int E, int
                                           tile_offsets, row_of_slot, token_of_row);
   MOE_CHECK_LAUNCH();
   return MOE_OK;
+}
+
+template <int KMAX>
+static int launch_route_count_index(const float *logits, int T, int E, int k, int32_t *topk_idx, float *topk_w,
+                                    int32_t *counts, int32_t *offsets, int32_t *tile_offsets, int32_t *row_of_slot,
+                                    int32_t *token_of_row, void *ws, cudaStream_t s, bool *launched) {
+  *launched = false;
+  const int nb = (int)index_blocks(T, k);
+  int per_sm = 0;   // every block must be resident at once (the blocks wait for the last one's scans)
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, route_count_index_kernel<KMAX>, kIdxThreads, 0) !=
+      cudaSuccess) {
+    (void)cudaGetLastError();
+    return MOE_OK;
+  }
+  if ((int64_t)per_sm * sm_count() < nb) return MOE_OK;
+  char *w = static_cast<char *>(ws);
+  IndexWs *iw = reinterpret_cast<IndexWs *>(w);
+  int32_t *acc = reinterpret_cast<int32_t *>(w + sizeof(IndexWs));
+  uint64_t *lookback = reinterpret_cast<uint64_t *>(w + sizeof(IndexWs) + acc_bytes(E) + kHookBytes);
+  // status, tickets, totals and every look-back word start at zero (the fault hook is cleared too)
+  MOE_TRY_CUDA(cudaMemsetAsync(w, 0, sizeof(IndexWs) + acc_bytes(E) + kHookBytes + (size_t)nb * E * sizeof(uint64_t),
+                               s));
+  route_count_index_kernel<KMAX><<<nb, kIdxThreads, 0, s>>>(logits, T, E, k, MOE_GROUP_ROWS, &iw->hdr, acc, lookback,
+                                                            topk_idx, topk_w, counts, offsets, tile_offsets,
+                                                            row_of_slot, token_of_row);
+  MOE_CHECK_LAUNCH();
+  *launched = true;
+  return MOE_OK;
+}
+
+extern "C" int moe_route_count_index(const float *logits, int T, int E, int k, int32_t *topk_idx, float *topk_w,
+                                     int32_t *counts, int32_t *offsets, int32_t *tile_offsets,
+                                     int32_t *row_of_slot, int32_t *token_of_row, void *ws, size_t ws_bytes,
+                                     moe_stream_t stream) {
+  if (T < 0 || E < 1 || E > MOE_MAX_EXPERTS || k < 1 || k > E || k > MOE_MAX_TOPK) return MOE_ERR_INVALID_ARG;
+  if ((int64_t)T * k >= (int64_t)1 << 31) return MOE_ERR_UNSUPPORTED;
+  if (!counts || !offsets || !tile_offsets || !token_of_row || !ws) return MOE_ERR_INVALID_ARG;
+  if (T > 0 && (!logits || !topk_idx || !topk_w || !row_of_slot)) return MOE_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(ws) & 255) != 0) return MOE_ERR_INVALID_ARG;
+  if (ws_bytes < moe_count_index_workspace_size(T, k, E)) return MOE_ERR_INVALID_ARG;
+  cudaStream_t s = (cudaStream_t)stream;
+  bool launched = false;
+  int rc = MOE_OK;
+  if (T > 0) {
+    if (k <= 2) rc = launch_route_count_index<2>(logits, T, E, k, topk_idx, topk_w, counts, offsets, tile_offsets,
+                                                 row_of_slot, token_of_row, ws, s, &launched);
+    else if (k <= 4) rc = launch_route_count_index<4>(logits, T, E, k, topk_idx, topk_w, counts, offsets,
+                                                      tile_offsets, row_of_slot, token_of_row, ws, s, &launched);
+    else if (k <= 8) rc = launch_route_count_index<8>(logits, T, E, k, topk_idx, topk_w, counts, offsets,
+                                                      tile_offsets, row_of_slot, token_of_row, ws, s, &launched);
+    else rc = launch_route_count_index<16>(logits, T, E, k, topk_idx, topk_w, counts, offsets, tile_offsets,
+                                           row_of_slot, token_of_row, ws, s, &launched);
+  }
+  if (rc || launched) return rc;
+  // too many blocks to be resident at once (or T = 0): the two calls, same results
+  if ((rc = moe_route_topk(logits, T, E, k, topk_idx, topk_w, stream))) return rc;
+  return moe_count_index(topk_idx, T, k, E, counts, offsets, tile_offsets, row_of_slot, token_of_row, ws, ws_bytes,
+                         stream);
 }
 
 extern "C" size_t moe_count_index_hook_offset(int E) {
