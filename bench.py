@@ -168,11 +168,13 @@ def run_ours(args):
         ev[0].record(stream)
         if args.router:
             L.moe_router_fwd(x, wr, w.k, layer.logits, layer.topk_idx, layer.topk_w, layer.ws_router)
-        else:
-            L.moe_route_topk(logits, w.k, layer.topk_idx, layer.topk_w)
-        ev[1].record(stream)
-        L.moe_count_index(layer.topk_idx, w.E, layer.counts, layer.offsets, layer.tile_offsets, layer.row_of_slot,
-                          layer.token_of_row, layer.ws_index)
+            ev[1].record(stream)
+            L.moe_count_index(layer.topk_idx, w.E, layer.counts, layer.offsets, layer.tile_offsets,
+                              layer.row_of_slot, layer.token_of_row, layer.ws_index)
+        else:   # routing, counting and index generation in one launch
+            L.moe_route_count_index(logits, w.k, layer.topk_idx, layer.topk_w, layer.counts, layer.offsets,
+                                    layer.tile_offsets, layer.row_of_slot, layer.token_of_row, layer.ws_index)
+            ev[1].record(stream)
         ev[2].record(stream)
         L.moe_permute(x, w.k, w.E, layer.row_of_slot, layer.counts, layer.tile_offsets, layer.x_perm)
         ev[3].record(stream)
@@ -209,7 +211,7 @@ def run_ours(args):
     if any(st):
         raise RuntimeError(f"device status after warm-up: {st}")
 
-    names = ["router_fwd" if args.router else "route_topk", "count_index", "permute", "grouped_ffn_fwd",
+    names = ["router_fwd" if args.router else "route_count_index", "count_index", "permute", "grouped_ffn_fwd",
              "combine_fwd", "combine_bwd", "grouped_ffn_bwd", "unpermute", "router_bwd"]
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(10)] for _ in range(args.steps)]
     t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -292,7 +294,7 @@ def run_ours(args):
         "router_bwd": (3 * w.T * w.d + 2 * w.E * w.d) * es + w.T * w.E * 4,
     }
     kern = {n: {"ms": round(v, 4)} for n, v in per.items()
-            if (bwd or n in names[:5]) and (args.router or n != "router_bwd")}
+            if (bwd or n in names[:5]) and (args.router or n not in ("router_bwd", "count_index"))}
     for n, b in mem_bytes.items():
         if n not in kern:
             continue

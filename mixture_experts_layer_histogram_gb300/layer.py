@@ -1,9 +1,10 @@
 """One MoE layer's expert computation on one GPU: resident buffers and the call sequence.
 
 Forward (one stream, no host synchronisation):
-  moe_route_topk   logits [T,E]        -> topk_idx [T,k], topk_w [T,k]
-   (or, given router weights: moe_router_fwd  x, w_router [E,d] -> logits, topk_idx, topk_w)
-  moe_count_index  topk_idx            -> counts, offsets, tile_offsets, row_of_slot, token_of_row
+  moe_route_count_index  logits [T,E]  -> topk_idx [T,k], topk_w [T,k], counts, offsets, tile_offsets,
+                                          row_of_slot, token_of_row   (routing + counting + indexing)
+   (or, given router weights: moe_router_fwd  x, w_router [E,d] -> logits, topk_idx, topk_w, then
+    moe_count_index  topk_idx -> counts, offsets, tile_offsets, row_of_slot, token_of_row)
   moe_permute      x [T,d]             -> x_perm [rows_max,d]
   moe_grouped_ffn_fwd                  -> ab [rows_max,2f], h [rows_max,f], y_perm [rows_max,d]
   moe_combine_fwd  y_perm, topk_w      -> out [T,d]
@@ -88,11 +89,12 @@ class MoELayer:
                 raise ValueError("w_router needs a layer built with router=True and logits=None")
             L.moe_router_fwd(x, w_router, self.k, self.logits, self.topk_idx, self.topk_w, self.ws_router, stream)
             self._x, self._w_router = x, w_router
-        else:
-            L.moe_route_topk(logits, self.k, self.topk_idx, self.topk_w, stream)
+            L.moe_count_index(self.topk_idx, self.E, self.counts, self.offsets, self.tile_offsets,
+                              self.row_of_slot, self.token_of_row, self.ws_index, stream)
+        else:   # routing, counting and index generation in one launch
+            L.moe_route_count_index(logits, self.k, self.topk_idx, self.topk_w, self.counts, self.offsets,
+                                    self.tile_offsets, self.row_of_slot, self.token_of_row, self.ws_index, stream)
             self._x = self._w_router = None
-        L.moe_count_index(self.topk_idx, self.E, self.counts, self.offsets, self.tile_offsets, self.row_of_slot,
-                          self.token_of_row, self.ws_index, stream)
         L.moe_permute(x, self.k, self.E, self.row_of_slot, self.counts, self.tile_offsets, self.x_perm, stream)
         L.moe_grouped_ffn_fwd(self.x_perm, w_gate_up, w_down, self.tile_offsets, self.ab, self.h, self.y_perm,
                               self.ws_ffn, stream)
@@ -143,7 +145,12 @@ class MoELayer:
 
     # kernels launched per pass, for the bench's launch count
     def launches(self, backward=True):
-        fwd = 1 + 2 + 1 + 2 + 1
+        if self._w_router is not None:
+            index = 1 + 2                     # router GEMM with top-k, count, index
+        else:                                 # one fused kernel while its blocks fit at once (2 per SM)
+            sms = torch.cuda.get_device_properties(self.device).multi_processor_count
+            index = 1 if -(-self.T * self.k // 1024) <= 2 * sms else 3
+        fwd = index + 1 + 2 + 1
         bwd = 1 + 4 + 1 + (1 if self.recompute else 0)
         if self._w_router is not None:
             bwd += 4   # prep, dx GEMM, dW GEMM, reduce
