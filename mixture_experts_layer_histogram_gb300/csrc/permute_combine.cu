@@ -1,6 +1,8 @@
 // Token permutation into the grouped layout, the weighted combine back to token order, and the
-// combine/routing backward. All three are HBM-bound row copies: one warp per token, 16-byte
-// vectors per lane, fp32 accumulation, the k row indices of a token held in lanes 0..k-1.
+// combine/routing backward. All three are HBM-bound row copies: a warp per token (per 2 KB segment
+// of a token's row in the combine), 16-byte vectors per lane, fp32 accumulation, the k row indices
+// of a token held in lanes 0..k-1; every lane issues the loads of all k rows of a chunk before it
+// uses any of them.
 //
 // "Scalable Pretraining of Large MoE LMs on Aurora", brief, section 核心方法: the generated indices
 // feed the grouped GEMM (permute) and the experts' outputs return to token order (combine); the
@@ -9,7 +11,7 @@
 
 namespace moe {
 
-constexpr int kRowThreads = 256;   // 8 warps, one token per warp per iteration
+constexpr int kRowThreads = 256;   // 8 warps, one work unit (token or row segment) per warp per iteration
 constexpr int kUnroll = 8;         // 16-byte vectors in flight per lane (a 4 KB row in one round trip)
 constexpr int kSegVecs = 128;      // combine: 16-byte vectors of a row per work unit (2 KB)
 

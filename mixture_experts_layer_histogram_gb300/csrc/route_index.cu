@@ -1,4 +1,5 @@
 // Routing (top-k + renormalised softmax), token counting and index generation.
+//   routing kernel : one thread per token, a sorted top-k list in registers (route_token).
 //
 // "Scalable Pretraining of Large MoE LMs on Aurora", brief, section 核心方法: FastSparseMoE counts
 // the tokens of each expert and generates their indices with GPU kernels before the grouped GEMM.
@@ -9,6 +10,9 @@
 //                  finds, per expert, how many earlier slots went to that expert with a decoupled
 //                  look-back over the preceding blocks (one 64-bit flag|value word per block and
 //                  expert), and scatters row_of_slot / token_of_row.
+//   route_count_index kernel : the routing, count and index kernels' work in one launch (each block
+//                  routes the tokens of its slots, then ranks, counts, looks back and scatters; the
+//                  blocks meet once, at the last block's scan of the totals).
 #include <math.h>
 
 #include "common.cuh"
