@@ -241,21 +241,19 @@ __device__ __forceinline__ void epilogue_tile(const Tile &t, const Params &p, ui
                             __uint_as_float(r[4 * q + 3]));
       }
     }
+  } else if constexpr (KIND != RDX) {
+#pragma unroll 1
+    for (int c = c0; c < c0 + BN / 2; c += 32) {
+      tmem_ld32(tbase + c, r);
+      tmem_ld_wait();
+#pragma unroll
+      for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+      es.put(mc0, t.n0 + c, yrow, v);
+    }
   } else {
     // RDX: with an addend, this row's previous dx, loaded in full (pre) before the accumulator was
     // ready (zeros past the tokens and past d)
-    const bool add = KIND == RDX && p.aux != nullptr;
-    if (KIND != RDX) {
-#pragma unroll 1
-      for (int c = c0; c < c0 + BN / 2; c += 32) {
-        tmem_ld32(tbase + c, r);
-        tmem_ld_wait();
-#pragma unroll
-        for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
-        es.put(mc0, t.n0 + c, yrow, v);
-      }
-      return;
-    }
+    const bool add = p.aux != nullptr;
 #pragma unroll
     for (int cc = 0; cc < BN / 64; ++cc) {
       const int c = c0 + 32 * cc;
@@ -263,7 +261,7 @@ __device__ __forceinline__ void epilogue_tile(const Tile &t, const Params &p, ui
       tmem_ld_wait();
 #pragma unroll
       for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
-      if (KIND == RDX && add) {
+      if (add) {
         float av[32];
 #pragma unroll
         for (int i = 0; i < 4; ++i) unpack_bf16x8(pre[(4 * cc + i) % pre_count(KIND)], av + 8 * i);
