@@ -313,7 +313,8 @@ __global__ void __launch_bounds__(kIdxThreads) index_kernel(const int32_t *__res
 // counts to the global totals and publishes its look-back aggregate. The last block to do so
 // computes the scans (counts, offsets, tile_offsets) and raises a flag; meanwhile every block looks
 // back over its predecessors, then waits for the flag (bounded, about 0.2 s) and scatters. The
-// wait needs every block resident at once; the host launches this kernel only when they fit.
+// wait needs every block resident at once: the host launches this kernel cooperatively, and only
+// when the whole grid fits on the GPU.
 template <int KMAX>
 __global__ void __launch_bounds__(kIdxThreads) route_count_index_kernel(
     const float *__restrict__ logits, int T, int E, int k, int BM, WsHeader *hdr, int32_t *acc,
@@ -497,10 +498,26 @@ static int launch_route_count_index(const float *logits, int T, int E, int k, in
   // status, tickets, totals and every look-back word start at zero (the fault hook is cleared too)
   MOE_TRY_CUDA(cudaMemsetAsync(w, 0, sizeof(IndexWs) + acc_bytes(E) + kHookBytes + (size_t)nb * E * sizeof(uint64_t),
                                s));
-  route_count_index_kernel<KMAX><<<nb, kIdxThreads, 0, s>>>(logits, T, E, k, MOE_GROUP_ROWS, &iw->hdr, acc, lookback,
-                                                            topk_idx, topk_w, counts, offsets, tile_offsets,
-                                                            row_of_slot, token_of_row);
-  MOE_CHECK_LAUNCH();
+  // A cooperative launch: CUDA starts the grid only when all of its blocks can be resident together,
+  // also while kernels from other streams (another layer, even another fused call) hold SMs, so the
+  // blocks' meeting point cannot wait on a block that is still queued.
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)nb, 1, 1);
+  cfg.blockDim = dim3(kIdxThreads, 1, 1);
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, route_count_index_kernel<KMAX>, logits, T, E, k, (int)MOE_GROUP_ROWS,
+                                           &iw->hdr, acc, lookback, topk_idx, topk_w, counts, offsets, tile_offsets,
+                                           row_of_slot, token_of_row);
+  if (e == cudaErrorCooperativeLaunchTooLarge) {   // the grid cannot be resident at once: two launches
+    (void)cudaGetLastError();
+    return MOE_OK;
+  }
+  MOE_TRY_CUDA(e);
   *launched = true;
   return MOE_OK;
 }
