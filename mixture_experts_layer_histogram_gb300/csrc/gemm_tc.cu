@@ -492,20 +492,23 @@ __global__ void __launch_bounds__(THREADS, 1)
 // leader's accumulator-empty barrier. Row-grouped kinds pair two consecutive row tiles of one
 // expert; when an expert has an odd number of row tiles, the second CTA of its last pair computes
 // rows past the expert and discards them.
-constexpr int P_BK = 64;                        // k depth of one ring stage (a multiple of 64)
-constexpr int P_KA = P_BK / 64;                 // 128-byte swizzle atoms along k per stage
-constexpr int P_STAGES = 6;
-constexpr int P_A_BYTES = BM * P_BK * 2;        // this CTA's 128 rows of A
-constexpr int P_B_BYTES = (BN / 2) * P_BK * 2;  // this CTA's half of B
-constexpr int P_STAGE_BYTES = P_A_BYTES + P_B_BYTES;
-// Per-kind layout: the DH kind gives one ring stage to per-warp buffers that bring the saved a, b
-// blocks in by TMA (two 4 KB buffers per epilogue warp, filled two 32-column chunks ahead).
+// Per-kind ring. Each stage costs the MMA thread one full-barrier wait and one commit, and the
+// producer one empty-barrier wait. With 64-deep stages those hand-offs held the tensor pipe to about
+// 72% of its rate even when no operand was loaded at all, so every kind runs 128-deep stages (three
+// of 64 KB). The exception is DH: its epilogue brings the saved a, b blocks in by TMA, into two 4 KB
+// buffers per epilogue warp (64 KB, filled two 32-column chunks ahead), which leaves room for five
+// 64-deep stages only; two 128-deep stages were slower.
 constexpr int DH_BUF_BYTES = 2 * EPI_BUF_BYTES;   // a block + b block of one chunk
 template <int KIND> struct PairCfg {
-  static constexpr int STAGES = KIND == DH ? P_STAGES - 1 : P_STAGES;
+  static constexpr int BKP = KIND == DH ? 64 : 128;       // k depth of one ring stage (a multiple of 64)
+  static constexpr int KA = BKP / 64;                     // 128-byte swizzle atoms along k per stage
+  static constexpr int A_BYTES = BM * BKP * 2;            // this CTA's 128 rows of A
+  static constexpr int B_BYTES = (BN / 2) * BKP * 2;      // this CTA's half of B
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+  static constexpr int STAGES = KIND == DH ? 5 : 3;
   static constexpr int EPI_BYTES = KIND == DH ? EPI_WARPS * 2 * DH_BUF_BYTES : EPI_STAGE_BYTES;
   static constexpr int NBARS = 2 * STAGES + 5 + (KIND == DH ? 2 * EPI_WARPS : 0);
-  static constexpr int SMEM = STAGES * P_STAGE_BYTES + EPI_BYTES + 1024 + 8 * NBARS + 16 + (MAX_E + 1) * 4;
+  static constexpr int SMEM = STAGES * STAGE_BYTES + EPI_BYTES + 1024 + 8 * NBARS + 16 + (MAX_E + 1) * 4;
   static_assert(SMEM <= 232448, "pair kernel shared memory exceeds 227 KB");
 };
 
@@ -528,7 +531,7 @@ __device__ __forceinline__ Tile decode_pair(int tile, const Params &p, const int
     t.m0 = (r / p.n_tiles) * (2 * BM) + rank * BM;
     t.n0 = (r % p.n_tiles) * BN;
     t.krow0 = toff[t.e] * BM;
-    t.kb = (toff[t.e + 1] - toff[t.e]) * (BM / P_BK);
+    t.kb = (toff[t.e + 1] - toff[t.e]) * (BM / PairCfg<KIND>::BKP);
   } else {
     const int pr = tile / p.n_tiles;
     const int nt = tile - pr * p.n_tiles;
@@ -543,7 +546,7 @@ __device__ __forceinline__ Tile decode_pair(int tile, const Params &p, const int
     valid = rt < toff[t.e + 1];
     t.m0 = rt * BM;
     t.n0 = nt * (KIND == GATEUP ? BN / 2 : BN);
-    t.kb = p.num_kb / P_KA;
+    t.kb = p.num_kb / PairCfg<KIND>::KA;
     t.krow0 = 0;
   }
   return t;
@@ -555,10 +558,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
                    const __grid_constant__ CUtensorMap tmC0, const __grid_constant__ CUtensorMap tmC1, const Params p) {
   constexpr bool A_MN = (KIND == WGRAD);
   constexpr bool B_MN = (KIND == DH || KIND == DGRAD || KIND == WGRAD);
-  constexpr int PS = PairCfg<KIND>::STAGES;
+  using Cfg = PairCfg<KIND>;
+  constexpr int PS = Cfg::STAGES;
+  constexpr int P_BK = Cfg::BKP, P_KA = Cfg::KA;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t *epi_smem = smem + PS * P_STAGE_BYTES;
+  uint8_t *epi_smem = smem + PS * Cfg::STAGE_BYTES;
   uint64_t *bars = reinterpret_cast<uint64_t *>(epi_smem + PairCfg<KIND>::EPI_BYTES);
   // bars: full[PS], empty[PS], tfull[2], tempty[2], mma_done, (DH) two load barriers per epilogue warp
   uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(bars + PairCfg<KIND>::NBARS);
@@ -666,9 +671,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
       bool ok = true;
       for (int kb = 0; kb < t.kb; ++kb) {
         if (!mbar_wait_cluster(empty_bar(stage), phase ^ 1u, abort_flag, p.hdr, 11)) { ok = false; break; }
-        const uint32_t sA = sbase + stage * P_STAGE_BYTES, sB = sA + P_A_BYTES;
+        const uint32_t sA = sbase + stage * Cfg::STAGE_BYTES, sB = sA + Cfg::A_BYTES;
         const uint32_t fb = mapa_shared(full_bar(stage), 0);   // the leader's full barrier
-        if (leader) mbar_expect_tx(full_bar(stage), 2 * P_STAGE_BYTES);
+        if (leader) mbar_expect_tx(full_bar(stage), 2 * Cfg::STAGE_BYTES);
         boxes(t, kb, sA, sB, fb);
         if (++stage == PS) { stage = 0; phase ^= 1u; }
       }
@@ -691,7 +696,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
       for (int kb = 0; kb < t.kb; ++kb) {
         if (!mbar_wait_cluster(full_bar(stage), phase, abort_flag, p.hdr, 13)) { ok = false; break; }
         tc_fence_after();
-        const uint32_t sA = sbase + stage * P_STAGE_BYTES, sB = sA + P_A_BYTES;
+        const uint32_t sA = sbase + stage * Cfg::STAGE_BYTES, sB = sA + Cfg::A_BYTES;
 #pragma unroll
         for (int kk = 0; kk < P_BK / 16; ++kk) {
           // K-major: atom kk/4 (128 rows x 128 B each), 32 B per 16-deep step inside the atom.
@@ -866,8 +871,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
 }
 
 // ----------------------------------------------------------------------------- host side -------
-constexpr uint32_t MN_BOX = P_BK;   // k rows of an MN-major TMA box (both kernels take P_BK == BK)
-static_assert(P_BK == BK, "the single-CTA and pair kernels share the MN-major tensor maps");
+// k rows of an MN-major TMA box: one ring stage of the kernel that reads it
+constexpr uint32_t MN_BOX = BK;   // single-CTA kernel
+template <int KIND> constexpr uint32_t pair_mn_box() { return (uint32_t)PairCfg<KIND>::BKP; }
 
 // The pair kernel pairs two row tiles of one expert, so an expert with an odd number of row tiles
 // computes one tile it throws away; with few row tiles per expert the single-CTA kernel wins.
@@ -975,7 +981,9 @@ int tc_grouped_ffn_bwd(const void *dy, const void *x_perm, const void *ab, const
   int rc;
   // dh = dy Wd[e] (Wd read MN-major), SwiGLU backward epilogue -> dab
   CUtensorMap mAB;   // the saved a, b blocks, read by the pair kernel's DH epilogue
-  if (!make_map(&mA, dy, rows_max, d, 128) || !make_map(&mB, wd, (uint64_t)E * d, f, MN_BOX) ||
+  const bool pair_dh = use_pair(DH, rows_max, E);
+  if (!make_map(&mA, dy, rows_max, d, 128) ||
+      !make_map(&mB, wd, (uint64_t)E * d, f, pair_dh ? pair_mn_box<DH>() : MN_BOX) ||
       !make_store_map(&mC, dab, rows_max, 2 * f) || !make_store_map(&mAB, ab, rows_max, 2 * f))
     return MOE_ERR_CUDA;
   p.n_tiles = f / BN;
@@ -985,10 +993,11 @@ int tc_grouped_ffn_bwd(const void *dy, const void *x_perm, const void *ab, const
   p.ld0 = 2 * (int64_t)f;
   p.aux = (const __nv_bfloat16 *)ab;
   p.ld_aux = 2 * (int64_t)f;
-  if ((rc = launch<DH>(mA, mB, mC, mAB, p, row_tiles * p.n_tiles, pair_rows * p.n_tiles, use_pair(DH, rows_max, E), s)))
+  if ((rc = launch<DH>(mA, mB, mC, mAB, p, row_tiles * p.n_tiles, pair_rows * p.n_tiles, pair_dh, s)))
     return rc;
   // dWd[e] = dy_e^T h_e
-  if (!make_map(&mA, dy, rows_max, d, MN_BOX) || !make_map(&mB, h, rows_max, f, MN_BOX) ||
+  // the weight-gradient kind always runs on the CTA-pair kernel, so its maps take that stage depth
+  if (!make_map(&mA, dy, rows_max, d, pair_mn_box<WGRAD>()) || !make_map(&mB, h, rows_max, f, pair_mn_box<WGRAD>()) ||
       !make_store_map(&mC, dwd, (uint64_t)E * d, f))
     return MOE_ERR_CUDA;
   p.m_tiles = d / BM;
@@ -1001,7 +1010,9 @@ int tc_grouped_ffn_bwd(const void *dy, const void *x_perm, const void *ab, const
                           (int64_t)E * (p.m_tiles / 2) * p.n_tiles, use_pair(WGRAD, rows_max, E), s)))
     return rc;
   // dx_perm = dab Wgu[e] (Wgu read MN-major)
-  if (!make_map(&mA, dab, rows_max, 2 * f, 128) || !make_map(&mB, wgu, (uint64_t)E * 2 * f, d, MN_BOX) ||
+  const bool pair_dg = use_pair(DGRAD, rows_max, E);
+  if (!make_map(&mA, dab, rows_max, 2 * f, 128) ||
+      !make_map(&mB, wgu, (uint64_t)E * 2 * f, d, pair_dg ? pair_mn_box<DGRAD>() : MN_BOX) ||
       !make_store_map(&mC, dx, rows_max, d))
     return MOE_ERR_CUDA;
   p.n_tiles = d / BN;
@@ -1009,11 +1020,11 @@ int tc_grouped_ffn_bwd(const void *dy, const void *x_perm, const void *ab, const
   p.b_rows_e = 2 * f;
   p.out0 = (__nv_bfloat16 *)dx;
   p.ld0 = d;
-  if ((rc = launch<DGRAD>(mA, mB, mC, mC, p, row_tiles * p.n_tiles, pair_rows * p.n_tiles,
-                          use_pair(DGRAD, rows_max, E), s)))
+  if ((rc = launch<DGRAD>(mA, mB, mC, mC, p, row_tiles * p.n_tiles, pair_rows * p.n_tiles, pair_dg, s)))
     return rc;
   // dWgu[e] = dab_e^T x_perm_e
-  if (!make_map(&mA, dab, rows_max, 2 * f, MN_BOX) || !make_map(&mB, x_perm, rows_max, d, MN_BOX) ||
+  if (!make_map(&mA, dab, rows_max, 2 * f, pair_mn_box<WGRAD>()) ||
+      !make_map(&mB, x_perm, rows_max, d, pair_mn_box<WGRAD>()) ||
       !make_store_map(&mC, dwgu, (uint64_t)E * 2 * f, d))
     return MOE_ERR_CUDA;
   p.m_tiles = 2 * f / BM;
