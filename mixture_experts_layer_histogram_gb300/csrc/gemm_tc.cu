@@ -3,10 +3,10 @@
 // "Scalable Pretraining of Large MoE LMs on Aurora", brief, section 核心方法: the experts'
 // computation is merged into one grouped GEMM; summary page, section 关键设计: with optimised
 // matrix multiplication and activation. Here one persistent, warp-specialised kernel per GEMM, in
-// two forms: the CTA-pair kernel further down (tcgen05.mma.cta_group::2 on a cluster of two CTAs,
-// 256 x 256 tiles, a 6-stage ring; every weight gradient, and the row-grouped kinds once the
-// experts average at least 4 row tiles) and the single-CTA kernel described here (smaller problems
-// and the router's kinds):
+// two forms. The CTA-pair kernel further down (tcgen05.mma.cta_group::2 on a cluster of two CTAs,
+// 256 x 256 tiles, three 128-deep ring stages, DH five 64-deep ones) runs every weight gradient,
+// and the row-grouped kinds once the experts average at least 4 row tiles. The single-CTA kernel
+// described here runs smaller problems and the router's kinds:
 //
 //   warp 0      TMA producer: 128B-swizzled tiles of A and B into a 4-stage shared-memory ring
 //   warp 1      allocates the 512 TMEM columns, issues tcgen05.mma (one thread), commits to barriers
