@@ -493,9 +493,9 @@ __global__ void __launch_bounds__(THREADS, 1)
 // expert; when an expert has an odd number of row tiles, the second CTA of its last pair computes
 // rows past the expert and discards them.
 // Per-kind ring. Each stage costs the MMA thread one full-barrier wait and one commit, and the
-// producer one empty-barrier wait. With 64-deep stages those hand-offs held the tensor pipe to about
-// 72% of its rate even when no operand was loaded at all, so every kind runs 128-deep stages (three
-// of 64 KB). The exception is DH: its epilogue brings the saved a, b blocks in by TMA, into two 4 KB
+// producer one empty-barrier wait. With 64-deep stages those hand-offs held the tensor pipe to
+// 72-77% of its rate whether or not any operand was loaded, so every kind runs 128-deep stages
+// (three of 64 KB). The exception is DH: its epilogue brings the saved a, b blocks in by TMA, into two 4 KB
 // buffers per epilogue warp (64 KB, filled two 32-column chunks ahead), which leaves room for five
 // 64-deep stages only; two 128-deep stages were slower.
 constexpr int DH_BUF_BYTES = 2 * EPI_BUF_BYTES;   // a block + b block of one chunk
