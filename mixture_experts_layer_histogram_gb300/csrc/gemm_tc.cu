@@ -670,7 +670,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
       const Tile t = decode_pair<KIND>(tile, p, toff, ptoff, (int)rank, valid);
       bool ok = true;
       for (int kb = 0; kb < t.kb; ++kb) {
-        if (!mbar_wait_cluster(empty_bar(stage), phase ^ 1u, abort_flag, p.hdr, 11)) { ok = false; break; }
+        if (!mbar_spin_cluster(empty_bar(stage), phase ^ 1u, abort_flag, p.hdr, 11)) { ok = false; break; }
         const uint32_t sA = sbase + stage * Cfg::STAGE_BYTES, sB = sA + Cfg::A_BYTES;
         const uint32_t fb = mapa_shared(full_bar(stage), 0);   // the leader's full barrier
         if (leader) mbar_expect_tx(full_bar(stage), 2 * Cfg::STAGE_BYTES);
@@ -694,7 +694,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
       const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
       bool ok = true;
       for (int kb = 0; kb < t.kb; ++kb) {
-        if (!mbar_wait_cluster(full_bar(stage), phase, abort_flag, p.hdr, 13)) { ok = false; break; }
+        if (!mbar_spin_cluster(full_bar(stage), phase, abort_flag, p.hdr, 13)) { ok = false; break; }
         tc_fence_after();
         const uint32_t sA = sbase + stage * Cfg::STAGE_BYTES, sB = sA + Cfg::A_BYTES;
 #pragma unroll

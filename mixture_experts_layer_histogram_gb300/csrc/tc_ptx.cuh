@@ -136,6 +136,33 @@ static __device__ __noinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t par
     }
   }
 }
+// The same bounded wait, polling with mbarrier.test_wait, which never suspends the thread. For the
+// two single-thread roles of the pair GEMM's ring (the TMA producer and the MMA issuer): a phase that
+// completes is seen a little sooner than through try_wait's suspend-and-wake, which shortens the
+// hand-off every ring stage costs.
+static __device__ __forceinline__ bool mbar_spin_cluster(uint32_t bar, uint32_t parity, volatile int *abort_flag,
+                                                         WsHeader *hdr, int where) {
+  const uint64_t t0 = global_ns();
+  for (uint32_t it = 0;; ++it) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    if (ok) return true;
+    if ((it & 255u) == 255u) {
+      if (*abort_flag) return false;
+      if (global_ns() - t0 > kWaitLimitNs) {
+        report(hdr, MOE_ERR_DEVICE_TIMEOUT, where);
+        *abort_flag = 1;
+        return false;
+      }
+    }
+  }
+}
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
   asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
 }
