@@ -31,7 +31,7 @@ METRIC = "MoE layer fwd+bwd tokens/s (E=64,k=8,d=2048); grouped-GEMM % BF16 peak
 
 # DRAM bytes (read + write) of the grouped-GEMM launches of one step, from an ncu capture of the
 # current kernels (profiles/dram_fwdbwd_t8192.md); None where no capture of the current kernels exists.
-GEMM_TRAFFIC = {"fwdbwd_t8192": 5818000000}
+GEMM_TRAFFIC = {"fwdbwd_t8192": 5816000000}
 DEFAULT_WORKLOAD = "fwdbwd_t8192"
 
 
