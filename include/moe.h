@@ -31,7 +31,11 @@
  * increasing token index); the rows after the last token of an expert up to the next multiple of
  * MOE_GROUP_ROWS are padding and are kept at zero. Every grouped buffer has
  * rows_max = moe_grouped_rows_max(T, k, E) rows; rows from tile_offsets[E] * MOE_GROUP_ROWS on are
- * never touched. With this layout every grouped-GEMM tile belongs to one expert and is full.
+ * never touched. With this layout every grouped-GEMM tile belongs to one expert and is full: no
+ * TMA box straddles two experts, no tile needs row masks, and the weight-gradient GEMMs may sum
+ * over an expert's padded rows because the padding is zero. This is why moe_permute and
+ * moe_combine_bwd take counts and tile_offsets (they write the padding zeros), why the grouped
+ * FFN calls take tile_offsets and rows_max, and why token_of_row has rows_max entries.
  */
 #ifndef MOE_LAYER_H_
 #define MOE_LAYER_H_
@@ -128,7 +132,10 @@ int moe_route_count_index(const float *logits, int T, int E, int k, int32_t *top
  *     MOE_STATIC_SCRATCH_BYTES return MOE_ERR_UNSUPPORTED (1 MiB covers T*k up to 2,095,104 slots at
  *     E = 64, or up to 523,264 slots at E = 256).
  *   - The first call on a device looks up the array's device address (cudaGetSymbolAddress) and
- *     caches it; make that first call before any stream capture on that device.
+ *     caches it for the life of the process; make that first call before any stream capture on
+ *     that device. The cache does not survive a reset of the device's primary context
+ *     (cudaDeviceReset): after one, the library reloads in a new context and the cached address is
+ *     stale, so do not call this entry point again in that process.
  *   - Every call on a device shares the one array: calls that overlap on the GPU (different streams
  *     without ordering between them) race and give wrong results. Each call clears what must start
  *     at zero, so consecutive calls are independent.

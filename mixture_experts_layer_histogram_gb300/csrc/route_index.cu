@@ -571,7 +571,9 @@ static __device__ __align__(256) unsigned char g_count_index_scratch[MOE_STATIC_
 #include <mutex>
 
 // The array's name is only a host-side stand-in, not a device address; each device's address is
-// looked up once (with that device current) and cached.
+// looked up once (with that device current) and cached for the life of the process. A reset of the
+// device's primary context (cudaDeviceReset) reloads the module at a new address, which this cache
+// does not follow: the header tells callers not to use this entry point after such a reset.
 static int static_scratch_address(void **out) {
   static std::mutex mu;
   static void *addr[64] = {};
