@@ -216,8 +216,8 @@ def run_ours(args):
         ev[2].record(stream)
         L.moe_permute(x, w.k, w.E, layer.row_of_slot, layer.counts, layer.tile_offsets, layer.x_perm)
         ev[3].record(stream)
-        L.moe_grouped_ffn_fwd(layer.x_perm, wgu, wd, layer.tile_offsets, layer.ab, layer.h, layer.y_perm,
-                              layer.ws_ffn)
+        L.moe_grouped_ffn_fwd(layer.x_perm, wgu, wd, layer.tile_offsets, layer.offsets, layer.ab, layer.h,
+                              layer.y_perm, layer.ws_ffn)
         ev[4].record(stream)
         L.moe_combine_fwd(layer.y_perm, layer.topk_w, layer.row_of_slot, w.T, w.k, layer.out)
         ev[5].record(stream)
@@ -229,8 +229,8 @@ def run_ours(args):
                           layer.tile_offsets, w.E, layer.dy_perm, layer.d_topk_w, layer.d_logits)
         ev[6].record(stream)
         (L.moe_grouped_ffn_bwd_recompute if args.recompute else L.moe_grouped_ffn_bwd)(
-            layer.dy_perm, layer.x_perm, layer.ab, layer.h, wgu, wd, layer.tile_offsets, layer.dab, layer.dx_perm,
-            layer.dw_gate_up, layer.dw_down, layer.ws_ffn)
+            layer.dy_perm, layer.x_perm, layer.ab, layer.h, wgu, wd, layer.tile_offsets, layer.offsets, layer.dab,
+            layer.dx_perm, layer.dw_gate_up, layer.dw_down, layer.ws_ffn)
         ev[7].record(stream)
         L.moe_combine_fwd(layer.dx_perm, None, layer.row_of_slot, w.T, w.k, layer.dx)
         ev[8].record(stream)

@@ -170,13 +170,16 @@ int moe_permute(const void *x, int dtype, int T, int d, int k, int E, const int3
  *   y_perm    [rows_max, d]   h Wd^T
  * GEMM1 fuses the SwiGLU gate into its epilogue; GEMM2 is a plain grouped GEMM. bf16: tcgen05
  * tensor cores, fp32 accumulation, outputs rounded to bf16; requires d % 256 == 0 and
- * f % 256 == 0. fp32: SIMT fp32 FMA, any d, f >= 1. tile_offsets comes from moe_count_index.
- * ws: moe_grouped_ffn_workspace_size(...) bytes (device status word). Padding rows produce zeros.
+ * f % 256 == 0. fp32: SIMT fp32 FMA, any d, f >= 1. tile_offsets and offsets come from
+ * moe_count_index: tile_offsets places each expert's rows, offsets gives how many are real (the
+ * bf16 kernels compute an expert's rows only up to the next multiple of 32 past its last token and
+ * write the rest of its padding as zeros). ws: moe_grouped_ffn_workspace_size(...) bytes (device
+ * status word). Padding rows come out as zeros.
  */
 size_t moe_grouped_ffn_workspace_size(int E, int d, int f, int64_t rows_max, int dtype, int backward);
 int moe_grouped_ffn_fwd(const void *x_perm, const void *w_gate_up, const void *w_down,
-                        const int32_t *tile_offsets, int E, int d, int f, int64_t rows_max, int dtype,
-                        void *ab, void *h, void *y_perm, void *ws, size_t ws_bytes, moe_stream_t stream);
+                        const int32_t *tile_offsets, const int32_t *offsets, int E, int d, int f, int64_t rows_max,
+                        int dtype, void *ab, void *h, void *y_perm, void *ws, size_t ws_bytes, moe_stream_t stream);
 
 /* ---------------------------------------------------------------------------------------------
  * Grouped expert FFN, backward (brief, sections 为什么值得记录 / 关键结果: the module is measured
@@ -189,9 +192,10 @@ int moe_grouped_ffn_fwd(const void *x_perm, const void *w_gate_up, const void *w
  * forward; gradients are written in the parameter dtype, accumulated in fp32.
  */
 int moe_grouped_ffn_bwd(const void *dy_perm, const void *x_perm, const void *ab, const void *h,
-                        const void *w_gate_up, const void *w_down, const int32_t *tile_offsets, int E,
-                        int d, int f, int64_t rows_max, int dtype, void *dab, void *dx_perm,
-                        void *dw_gate_up, void *dw_down, void *ws, size_t ws_bytes, moe_stream_t stream);
+                        const void *w_gate_up, const void *w_down, const int32_t *tile_offsets,
+                        const int32_t *offsets, int E, int d, int f, int64_t rows_max, int dtype, void *dab,
+                        void *dx_perm, void *dw_gate_up, void *dw_down, void *ws, size_t ws_bytes,
+                        moe_stream_t stream);
 
 /* ---------------------------------------------------------------------------------------------
  * Backward with recomputation (brief, section 核心方法: selective activation checkpointing, which
@@ -202,9 +206,9 @@ int moe_grouped_ffn_bwd(const void *dy_perm, const void *x_perm, const void *ab,
  * layer's backward; the cost is one more GEMM1 (4 M d f FLOP).
  */
 int moe_grouped_ffn_bwd_recompute(const void *dy_perm, const void *x_perm, void *ab, void *h, const void *w_gate_up,
-                                  const void *w_down, const int32_t *tile_offsets, int E, int d, int f,
-                                  int64_t rows_max, int dtype, void *dab, void *dx_perm, void *dw_gate_up,
-                                  void *dw_down, void *ws, size_t ws_bytes, moe_stream_t stream);
+                                  const void *w_down, const int32_t *tile_offsets, const int32_t *offsets, int E,
+                                  int d, int f, int64_t rows_max, int dtype, void *dab, void *dx_perm,
+                                  void *dw_gate_up, void *dw_down, void *ws, size_t ws_bytes, moe_stream_t stream);
 
 /* ---------------------------------------------------------------------------------------------
  * Weighted un-permute (combine) back to token order:

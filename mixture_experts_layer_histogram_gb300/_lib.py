@@ -35,10 +35,10 @@ _SIGS = {
     "moe_route_count_index": (_I, [_P, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]),
     "moe_permute": (_I, [_P, _I, _I, _I, _I, _I, _P, _P, _P, _I64, _P, _P]),
     "moe_grouped_ffn_workspace_size": (_SZ, [_I, _I, _I, _I64, _I, _I]),
-    "moe_grouped_ffn_fwd": (_I, [_P, _P, _P, _P, _I, _I, _I, _I64, _I, _P, _P, _P, _P, _SZ, _P]),
-    "moe_grouped_ffn_bwd": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I64, _I, _P, _P, _P, _P, _P, _SZ, _P]),
-    "moe_grouped_ffn_bwd_recompute": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I64, _I, _P, _P, _P, _P, _P, _SZ,
-                                           _P]),
+    "moe_grouped_ffn_fwd": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I64, _I, _P, _P, _P, _P, _SZ, _P]),
+    "moe_grouped_ffn_bwd": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I64, _I, _P, _P, _P, _P, _P, _SZ, _P]),
+    "moe_grouped_ffn_bwd_recompute": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I64, _I, _P, _P, _P, _P, _P,
+                                           _SZ, _P]),
     "moe_combine_fwd": (_I, [_P, _P, _P, _I, _I, _I, _I64, _I, _P, _P]),
     "moe_combine_bwd": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I64, _I, _P, _P, _P, _P]),
     "moe_router_workspace_size": (_SZ, [_I, _I, _I, _I]),
@@ -153,27 +153,29 @@ def moe_grouped_ffn_workspace_size(E, d, f, rows_max, dtype, backward):
     return int(lib().moe_grouped_ffn_workspace_size(E, d, f, rows_max, dtype, int(backward)))
 
 
-def moe_grouped_ffn_fwd(x_perm, w_gate_up, w_down, tile_offsets, ab, h, y_perm, ws, stream=None):
+def moe_grouped_ffn_fwd(x_perm, w_gate_up, w_down, tile_offsets, offsets, ab, h, y_perm, ws, stream=None):
     E, twof, d = w_gate_up.shape
     _ok("moe_grouped_ffn_fwd", lib().moe_grouped_ffn_fwd(
-        _p(x_perm), _p(w_gate_up), _p(w_down), _p(tile_offsets), E, d, twof // 2, x_perm.shape[0],
+        _p(x_perm), _p(w_gate_up), _p(w_down), _p(tile_offsets), _p(offsets), E, d, twof // 2, x_perm.shape[0],
         dtype_code(x_perm.dtype), _p(ab), _p(h), _p(y_perm), _p(ws), ws.numel() * ws.element_size(), _s(stream)))
 
 
-def moe_grouped_ffn_bwd(dy_perm, x_perm, ab, h, w_gate_up, w_down, tile_offsets, dab, dx_perm, dw_gate_up, dw_down,
-                        ws, stream=None):
+def moe_grouped_ffn_bwd(dy_perm, x_perm, ab, h, w_gate_up, w_down, tile_offsets, offsets, dab, dx_perm, dw_gate_up,
+                        dw_down, ws, stream=None):
     E, twof, d = w_gate_up.shape
     _ok("moe_grouped_ffn_bwd", lib().moe_grouped_ffn_bwd(
-        _p(dy_perm), _p(x_perm), _p(ab), _p(h), _p(w_gate_up), _p(w_down), _p(tile_offsets), E, d, twof // 2,
+        _p(dy_perm), _p(x_perm), _p(ab), _p(h), _p(w_gate_up), _p(w_down), _p(tile_offsets), _p(offsets), E, d,
+        twof // 2,
         x_perm.shape[0], dtype_code(x_perm.dtype), _p(dab), _p(dx_perm), _p(dw_gate_up), _p(dw_down), _p(ws),
         ws.numel() * ws.element_size(), _s(stream)))
 
 
-def moe_grouped_ffn_bwd_recompute(dy_perm, x_perm, ab, h, w_gate_up, w_down, tile_offsets, dab, dx_perm, dw_gate_up,
-                                  dw_down, ws, stream=None):
+def moe_grouped_ffn_bwd_recompute(dy_perm, x_perm, ab, h, w_gate_up, w_down, tile_offsets, offsets, dab, dx_perm,
+                                  dw_gate_up, dw_down, ws, stream=None):
     E, twof, d = w_gate_up.shape
     _ok("moe_grouped_ffn_bwd_recompute", lib().moe_grouped_ffn_bwd_recompute(
-        _p(dy_perm), _p(x_perm), _p(ab), _p(h), _p(w_gate_up), _p(w_down), _p(tile_offsets), E, d, twof // 2,
+        _p(dy_perm), _p(x_perm), _p(ab), _p(h), _p(w_gate_up), _p(w_down), _p(tile_offsets), _p(offsets), E, d,
+        twof // 2,
         x_perm.shape[0], dtype_code(x_perm.dtype), _p(dab), _p(dx_perm), _p(dw_gate_up), _p(dw_down), _p(ws),
         ws.numel() * ws.element_size(), _s(stream)))
 

@@ -16,7 +16,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libmoe.so")
-SOURCES = ["route_index.cu", "permute_combine.cu", "gemm_simt.cu", "gemm_tc.cu", "router.cu", "api.cu"]
+SOURCES = ["route_index.cu", "permute_combine.cu", "gemm_simt.cu", "gemm_tc.cu", "gemm_rows.cu", "router.cu", "api.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

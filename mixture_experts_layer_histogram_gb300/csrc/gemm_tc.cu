@@ -924,50 +924,30 @@ static int launch(const CUtensorMap &a, const CUtensorMap &b, const CUtensorMap 
 
 }  // namespace tc
 
-// Entry points used by the C ABI (gemm_api.cu).
-int tc_grouped_ffn_fwd(const void *x_perm, const void *wgu, const void *wd, const int32_t *tile_offsets, int E, int d,
-                       int f, int64_t rows_max, void *ab, void *h, void *y, WsHeader *hdr, cudaStream_t s) {
-  using namespace tc;
-  CUtensorMap mA, mB, mC0, mC1;
-  Params p{};
-  p.tile_offsets = tile_offsets;
-  p.hdr = hdr;
-  p.E = E;
-  p.d = d;
-  p.f = f;
-  const int64_t row_tiles = rows_max / BM;
-  const int64_t pair_rows = (row_tiles + 1) / 2 + E;   // upper bound on pair rows (one odd tile per expert)
+// Row-grouped kinds (gemm_rows.cu): weights as A, tokens as B, on CTA pairs.
+int rows_gateup(const void *x_perm, const void *wgu, const int32_t *tile_offsets, const int32_t *offsets, int E, int d,
+                int f, int64_t rows_max, void *ab, void *h, WsHeader *hdr, cudaStream_t s);
+int rows_down(const void *h, const void *wd, const int32_t *tile_offsets, const int32_t *offsets, int E, int d, int f,
+              int64_t rows_max, void *y, WsHeader *hdr, cudaStream_t s);
+int rows_dh(const void *dy, const void *wd, const void *ab, const int32_t *tile_offsets, const int32_t *offsets, int E,
+            int d, int f, int64_t rows_max, void *dab, WsHeader *hdr, cudaStream_t s);
+int rows_dgrad(const void *dab, const void *wgu, const int32_t *tile_offsets, const int32_t *offsets, int E, int d,
+               int f, int64_t rows_max, void *dx, WsHeader *hdr, cudaStream_t s);
+
+// Entry points used by the C ABI (api.cu).
+int tc_grouped_ffn_fwd(const void *x_perm, const void *wgu, const void *wd, const int32_t *tile_offsets,
+                       const int32_t *offsets, int E, int d, int f, int64_t rows_max, void *ab, void *h, void *y,
+                       WsHeader *hdr, cudaStream_t s) {
   // GEMM1: [a | b] = x_perm Wgu^T, SwiGLU epilogue
-  if (!make_map(&mA, x_perm, rows_max, d, 128) || !make_map(&mB, wgu, (uint64_t)E * 2 * f, d, 128) ||
-      !make_store_map(&mC0, ab, rows_max, 2 * f) || !make_store_map(&mC1, h, rows_max, f))
-    return MOE_ERR_CUDA;
-  p.n_tiles = f / (BN / 2);
-  p.num_kb = d / BK;
-  p.b_rows_e = 2 * f;
-  p.out0 = (__nv_bfloat16 *)ab;
-  p.ld0 = 2 * (int64_t)f;
-  p.out1 = (__nv_bfloat16 *)h;
-  p.ld1 = f;
-  int rc = launch<GATEUP>(mA, mB, mC0, mC1, p, row_tiles * p.n_tiles, pair_rows * p.n_tiles,
-                          use_pair(GATEUP, rows_max, E), s);
+  int rc = rows_gateup(x_perm, wgu, tile_offsets, offsets, E, d, f, rows_max, ab, h, hdr, s);
   if (rc || y == nullptr) return rc;   // y == nullptr: GEMM1 only (recompute of ab, h)
   // GEMM2: y = h Wd^T
-  if (!make_map(&mA, h, rows_max, f, 128) || !make_map(&mB, wd, (uint64_t)E * d, f, 128) ||
-      !make_store_map(&mC0, y, rows_max, d))
-    return MOE_ERR_CUDA;
-  p.n_tiles = d / BN;
-  p.num_kb = f / BK;
-  p.b_rows_e = d;
-  p.out0 = (__nv_bfloat16 *)y;
-  p.ld0 = d;
-  p.out1 = nullptr;
-  return launch<DOWN>(mA, mB, mC0, mC0, p, row_tiles * p.n_tiles, pair_rows * p.n_tiles, use_pair(DOWN, rows_max, E),
-                      s);
+  return rows_down(h, wd, tile_offsets, offsets, E, d, f, rows_max, y, hdr, s);
 }
 
 int tc_grouped_ffn_bwd(const void *dy, const void *x_perm, const void *ab, const void *h, const void *wgu,
-                       const void *wd, const int32_t *tile_offsets, int E, int d, int f, int64_t rows_max, void *dab,
-                       void *dx, void *dwgu, void *dwd, WsHeader *hdr, cudaStream_t s) {
+                       const void *wd, const int32_t *tile_offsets, const int32_t *offsets, int E, int d, int f,
+                       int64_t rows_max, void *dab, void *dx, void *dwgu, void *dwd, WsHeader *hdr, cudaStream_t s) {
   using namespace tc;
   CUtensorMap mA, mB, mC;
   Params p{};
@@ -976,27 +956,10 @@ int tc_grouped_ffn_bwd(const void *dy, const void *x_perm, const void *ab, const
   p.E = E;
   p.d = d;
   p.f = f;
-  const int64_t row_tiles = rows_max / BM;
-  const int64_t pair_rows = (row_tiles + 1) / 2 + E;
   int rc;
   // dh = dy Wd[e] (Wd read MN-major), SwiGLU backward epilogue -> dab
-  CUtensorMap mAB;   // the saved a, b blocks, read by the pair kernel's DH epilogue
-  const bool pair_dh = use_pair(DH, rows_max, E);
-  if (!make_map(&mA, dy, rows_max, d, 128) ||
-      !make_map(&mB, wd, (uint64_t)E * d, f, pair_dh ? pair_mn_box<DH>() : MN_BOX) ||
-      !make_store_map(&mC, dab, rows_max, 2 * f) || !make_store_map(&mAB, ab, rows_max, 2 * f))
-    return MOE_ERR_CUDA;
-  p.n_tiles = f / BN;
-  p.num_kb = d / BK;
-  p.b_rows_e = d;
-  p.out0 = (__nv_bfloat16 *)dab;
-  p.ld0 = 2 * (int64_t)f;
-  p.aux = (const __nv_bfloat16 *)ab;
-  p.ld_aux = 2 * (int64_t)f;
-  if ((rc = launch<DH>(mA, mB, mC, mAB, p, row_tiles * p.n_tiles, pair_rows * p.n_tiles, pair_dh, s)))
-    return rc;
-  // dWd[e] = dy_e^T h_e
-  // the weight-gradient kind always runs on the CTA-pair kernel, so its maps take that stage depth
+  if ((rc = rows_dh(dy, wd, ab, tile_offsets, offsets, E, d, f, rows_max, dab, hdr, s))) return rc;
+  // dWd[e] = dy_e^T h_e (the weight-gradient kind runs on the CTA-pair kernel, whose stage depth its maps take)
   if (!make_map(&mA, dy, rows_max, d, pair_mn_box<WGRAD>()) || !make_map(&mB, h, rows_max, f, pair_mn_box<WGRAD>()) ||
       !make_store_map(&mC, dwd, (uint64_t)E * d, f))
     return MOE_ERR_CUDA;
@@ -1005,23 +968,11 @@ int tc_grouped_ffn_bwd(const void *dy, const void *x_perm, const void *ab, const
   p.out0 = (__nv_bfloat16 *)dwd;
   p.ld0 = f;
   p.out_e_stride = (int64_t)d * f;
-  p.aux = nullptr;
   if ((rc = launch<WGRAD>(mA, mB, mC, mC, p, (int64_t)E * p.m_tiles * p.n_tiles,
-                          (int64_t)E * (p.m_tiles / 2) * p.n_tiles, use_pair(WGRAD, rows_max, E), s)))
+                          (int64_t)E * (p.m_tiles / 2) * p.n_tiles, true, s)))
     return rc;
   // dx_perm = dab Wgu[e] (Wgu read MN-major)
-  const bool pair_dg = use_pair(DGRAD, rows_max, E);
-  if (!make_map(&mA, dab, rows_max, 2 * f, 128) ||
-      !make_map(&mB, wgu, (uint64_t)E * 2 * f, d, pair_dg ? pair_mn_box<DGRAD>() : MN_BOX) ||
-      !make_store_map(&mC, dx, rows_max, d))
-    return MOE_ERR_CUDA;
-  p.n_tiles = d / BN;
-  p.num_kb = 2 * f / BK;
-  p.b_rows_e = 2 * f;
-  p.out0 = (__nv_bfloat16 *)dx;
-  p.ld0 = d;
-  if ((rc = launch<DGRAD>(mA, mB, mC, mC, p, row_tiles * p.n_tiles, pair_rows * p.n_tiles, pair_dg, s)))
-    return rc;
+  if ((rc = rows_dgrad(dab, wgu, tile_offsets, offsets, E, d, f, rows_max, dx, hdr, s))) return rc;
   // dWgu[e] = dab_e^T x_perm_e
   if (!make_map(&mA, dab, rows_max, 2 * f, pair_mn_box<WGRAD>()) ||
       !make_map(&mB, x_perm, rows_max, d, pair_mn_box<WGRAD>()) ||
@@ -1033,7 +984,7 @@ int tc_grouped_ffn_bwd(const void *dy, const void *x_perm, const void *ab, const
   p.ld0 = d;
   p.out_e_stride = (int64_t)2 * f * d;
   return launch<WGRAD>(mA, mB, mC, mC, p, (int64_t)E * p.m_tiles * p.n_tiles, (int64_t)E * (p.m_tiles / 2) * p.n_tiles,
-                       use_pair(WGRAD, rows_max, E), s);
+                       true, s);
 }
 
 // Router backward GEMMs (router.cu prepares dl16, the bf16 copy of d_logits [t_pad, ek] with zero

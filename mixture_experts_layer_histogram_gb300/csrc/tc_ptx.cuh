@@ -191,5 +191,43 @@ __device__ __forceinline__ void mma_commit_pair(uint32_t bar, uint16_t mask) {
       : "memory");
 }
 
+// 5D tensor TMA into this CTA's shared memory, completing bytes on an mbarrier that may live in the
+// peer CTA (the gate/up weight view of the row-grouped GEMM).
+__device__ __forceinline__ void tma_load_5d_pair(uint32_t dst, const CUtensorMap *map, int c0, int c1, int c2, int c3,
+                                                 int c4, uint32_t bar_cluster_addr) {
+  asm volatile(
+      "cp.async.bulk.tensor.5d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, "
+      "%4, %5, %6}], [%7];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4), "r"(bar_cluster_addr)
+      : "memory");
+}
+
+// tcgen05.ld of 16 TMEM lanes x 32 columns (four 16x256b blocks): thread T receives, for column
+// block c (8 columns), r[4c + 0..1] = lane T/4, columns 8c + 2 (T % 4) + {0, 1}, and r[4c + 2..3] =
+// lane T/4 + 8, the same columns (the register layout of an mma.m16n8 accumulator fragment).
+__device__ __forceinline__ void tmem_ld16x256b_x4(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.16x256b.x4.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
+        "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+}
+
+// Four 8x8 bf16 matrices in mma fragment layout (thread T: row T/4, columns 2 (T % 4) + {0, 1}),
+// stored transposed: row i of matrix m goes to the 16-byte shared-memory row whose address thread
+// 8m + i supplies, and holds column i of the fragment.
+__device__ __forceinline__ void stmatrix_t4(uint32_t addr, uint32_t m0, uint32_t m1, uint32_t m2, uint32_t m3) {
+  asm volatile("stmatrix.sync.aligned.m8n8.x4.trans.shared.b16 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(m0), "r"(m1),
+               "r"(m2), "r"(m3)
+               : "memory");
+}
+// The inverse of stmatrix_t4: the fragments of four 8x8 matrices read transposed from shared memory.
+__device__ __forceinline__ void ldmatrix_t4(uint32_t addr, uint32_t (&m)[4]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(m[0]), "=r"(m[1]), "=r"(m[2]), "=r"(m[3])
+               : "r"(addr)
+               : "memory");
+}
+
 }  // namespace tc
 }  // namespace moe

@@ -48,5 +48,24 @@ inline bool make_store_map(CUtensorMap *m, const void *base, uint64_t rows, uint
   return encode_map(m, base, rows, cols, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B);
 }
 
+// epilogue stores of 16-column blocks: 16 x 32 boxes (32-byte rows), 32-byte swizzle
+inline bool make_store_map16(CUtensorMap *m, const void *base, uint64_t rows, uint64_t cols) {
+  return encode_map(m, base, rows, cols, 16, 32, CU_TENSOR_MAP_SWIZZLE_32B);
+}
+// The gate/up weights Wgu [E, 2f, d] as a 5D view (k, row r, gate/up u, group g, expert e) ->
+// Wgu[e][u f + 8 g + r][k]. One box (64 k x 8 rows x 2 x 8 groups) lands in shared memory as 128
+// rows in which each group's 8 gate rows are followed by the same group's 8 up rows.
+inline bool make_gateup_map(CUtensorMap *m, const void *wgu, uint64_t E, uint64_t f, uint64_t d) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[5] = {d, 8, 2, f / 8, E};
+  cuuint64_t strides[4] = {d * 2, f * d * 2, 8 * d * 2, 2 * f * d * 2};
+  cuuint32_t box[5] = {64, 8, 2, 8, 1};
+  cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void *>(wgu), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 }  // namespace tc
 }  // namespace moe

@@ -96,8 +96,8 @@ class MoELayer:
                                     self.tile_offsets, self.row_of_slot, self.token_of_row, self.ws_index, stream)
             self._x = self._w_router = None
         L.moe_permute(x, self.k, self.E, self.row_of_slot, self.counts, self.tile_offsets, self.x_perm, stream)
-        L.moe_grouped_ffn_fwd(self.x_perm, w_gate_up, w_down, self.tile_offsets, self.ab, self.h, self.y_perm,
-                              self.ws_ffn, stream)
+        L.moe_grouped_ffn_fwd(self.x_perm, w_gate_up, w_down, self.tile_offsets, self.offsets, self.ab, self.h,
+                              self.y_perm, self.ws_ffn, stream)
         L.moe_combine_fwd(self.y_perm, self.topk_w, self.row_of_slot, self.T, self.k, self.out, stream)
         return self.out
 
@@ -107,8 +107,8 @@ class MoELayer:
         L.moe_combine_bwd(grad_out, self.y_perm, self.topk_w, self.topk_idx, self.row_of_slot, self.counts,
                           self.tile_offsets, self.E, self.dy_perm, self.d_topk_w, self.d_logits, stream)
         bwd = L.moe_grouped_ffn_bwd_recompute if self.recompute else L.moe_grouped_ffn_bwd
-        bwd(self.dy_perm, self.x_perm, self.ab, self.h, w_gate_up, w_down, self.tile_offsets, self.dab, self.dx_perm,
-            self.dw_gate_up, self.dw_down, self.ws_ffn, stream)
+        bwd(self.dy_perm, self.x_perm, self.ab, self.h, w_gate_up, w_down, self.tile_offsets, self.offsets, self.dab,
+            self.dx_perm, self.dw_gate_up, self.dw_down, self.ws_ffn, stream)
         L.moe_combine_fwd(self.dx_perm, None, self.row_of_slot, self.T, self.k, self.dx, stream)
         res = dict(dx=self.dx, d_logits=self.d_logits, d_topk_w=self.d_topk_w, dw_gate_up=self.dw_gate_up,
                    dw_down=self.dw_down)

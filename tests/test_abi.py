@@ -85,11 +85,16 @@ def test_invalid_arguments_are_rejected_on_the_host(L):
     assert L.moe_permute(FAKE, 7, 64, 64, 2, 8, FAKE, FAKE, FAKE, rm, FAKE, NULL) == -1
     # grouped FFN: bf16 needs d, f multiples of 256; rows_max multiple of 128; workspace present
     ws = L.moe_grouped_ffn_workspace_size(8, 128, 256, rm, 1, 1)
-    assert L.moe_grouped_ffn_fwd(FAKE, FAKE, FAKE, FAKE, 8, 128, 256, rm, 1, FAKE, FAKE, FAKE, FAKE, ws, NULL) == -2
-    assert L.moe_grouped_ffn_fwd(FAKE, FAKE, FAKE, FAKE, 8, 256, 256, rm + 1, 1, FAKE, FAKE, FAKE, FAKE, ws, NULL) == -1
-    assert L.moe_grouped_ffn_fwd(FAKE, FAKE, FAKE, FAKE, 8, 256, 256, rm, 1, FAKE, FAKE, FAKE, NULL, ws, NULL) == -1
-    assert L.moe_grouped_ffn_bwd(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 8, 256, 100, rm, 1, FAKE, FAKE, FAKE, FAKE,
-                                 FAKE, ws, NULL) == -2
+    assert L.moe_grouped_ffn_fwd(FAKE, FAKE, FAKE, FAKE, FAKE, 8, 128, 256, rm, 1, FAKE, FAKE, FAKE, FAKE, ws,
+                                 NULL) == -2
+    assert L.moe_grouped_ffn_fwd(FAKE, FAKE, FAKE, FAKE, FAKE, 8, 256, 256, rm + 1, 1, FAKE, FAKE, FAKE, FAKE, ws,
+                                 NULL) == -1
+    assert L.moe_grouped_ffn_fwd(FAKE, FAKE, FAKE, FAKE, FAKE, 8, 256, 256, rm, 1, FAKE, FAKE, FAKE, NULL, ws,
+                                 NULL) == -1
+    assert L.moe_grouped_ffn_fwd(FAKE, FAKE, FAKE, FAKE, NULL, 8, 256, 256, rm, 1, FAKE, FAKE, FAKE, FAKE, ws,
+                                 NULL) == -1                                   # offsets missing
+    assert L.moe_grouped_ffn_bwd(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 8, 256, 100, rm, 1, FAKE, FAKE, FAKE,
+                                 FAKE, FAKE, ws, NULL) == -2
     # combine: misaligned output, k out of range
     assert L.moe_combine_fwd(FAKE, FAKE, FAKE, 64, 64, 2, rm, 1, ctypes.c_void_p((1 << 20) + 2), NULL) == -1
     assert L.moe_combine_fwd(FAKE, FAKE, FAKE, 64, 64, 0, rm, 1, FAKE, NULL) == -1

@@ -5,6 +5,8 @@ ragged and empty experts, so every kind's tile decoding, tails and epilogue are 
 Each reference uses the library's own previous-stage output as its input (e.g. y is checked
 against h_gpu Wd^T), so a failure names the kind that is wrong.
 """
+import itertools
+
 import pytest
 import torch
 
@@ -13,28 +15,26 @@ from helpers import grouped_rows, rel_err, tile_offsets_from_counts, tol_for
 pytestmark = pytest.mark.gpu
 
 CASES = [
-    # E, d, f, counts (ragged, empty, a single row, exact multiples of the tile), kernel path. With
-    # fewer than 4 row tiles per expert on average (rows_max / 128 < 4 E) the row-grouped kinds run
-    # on the single-CTA kernel, otherwise on the CTA-pair kernel (odd tile counts leave a half-used
-    # last pair). The weight-gradient kind always runs on the pair kernel.
-    (4, 512, 512, [300, 0, 129, 1], "single"),
-    (3, 256, 256, [128, 256, 5], "single"),
-    (2, 256, 768, [1, 383], "single"),
-    (4, 512, 512, [300, 0, 129, 1], "pair"),
-    (2, 512, 512, [700, 1000], "pair"),
-    (3, 256, 512, [1100, 0, 513], "pair"),
-    (4, 512, 256, [1024, 1, 640, 897], "pair"),
+    # E, d, f, counts: ragged, empty, single-row and tile-multiple experts. The row-grouped kinds
+    # split an expert's c rows into ceil(c / 256) token tiles of multiples of 32 (e.g. 700 rows ->
+    # 256 + 224 + 224, 257 -> 160 + 128, 2049 -> 9 tiles), so these counts cover one- and many-tile
+    # experts, uneven splits, and tails of 1..31 rows past a multiple of 32.
+    (4, 512, 512, [300, 0, 129, 1]),
+    (3, 256, 256, [128, 256, 5]),
+    (2, 256, 768, [1, 383]),
+    (2, 512, 512, [700, 1000]),
+    (3, 256, 512, [1100, 0, 513]),
+    (4, 512, 256, [1024, 1, 640, 897]),
+    (5, 256, 256, [257, 31, 32, 33, 2049]),
+    (1, 768, 256, [4095]),
 ]
 
 
-def _setup(E, d, f, counts, dtype, path, seed=0):
+def _setup(E, d, f, counts, dtype, seed=0):
     from mixture_experts_layer_histogram_gb300 import _lib as L
     g = torch.Generator().manual_seed(seed)
     toff = tile_offsets_from_counts(counts)
     R = toff[-1] * 128 + 256          # a few unused rows after the last group
-    if path == "pair":                 # the kernel choice follows rows_max / (128 E), as in a real layer
-        R = max(R, 4 * 128 * E)
-    assert (R // 128 >= 4 * E) == (path == "pair")
     rows = grouped_rows(counts)
     real = torch.zeros(R, dtype=torch.bool)
     for rr in rows:
@@ -47,6 +47,7 @@ def _setup(E, d, f, counts, dtype, path, seed=0):
     t = dict(x=x, dy=dy, wgu=wgu, wd=wd)
     gt = {k: v.to(dev) for k, v in t.items()}
     gt["toff"] = torch.tensor(toff, dtype=torch.int32, device=dev)
+    gt["off"] = torch.tensor([0] + list(itertools.accumulate(counts)), dtype=torch.int32, device=dev)
     ws = torch.zeros(L.moe_grouped_ffn_workspace_size(E, d, f, R, L.dtype_code(dtype), 1), dtype=torch.uint8,
                      device=dev)
     act = dict(dtype=dtype, device=dev)
@@ -58,12 +59,12 @@ def _setup(E, d, f, counts, dtype, path, seed=0):
 
 
 @pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
-@pytest.mark.parametrize("E,d,f,counts,path", CASES)
-def test_grouped_gemm_kinds(E, d, f, counts, path, dtype):
-    L, t, gt, rows, ws, o = _setup(E, d, f, counts, dtype, path)
-    L.moe_grouped_ffn_fwd(gt["x"], gt["wgu"], gt["wd"], gt["toff"], o["ab"], o["h"], o["y"], ws)
-    L.moe_grouped_ffn_bwd(gt["dy"], gt["x"], o["ab"], o["h"], gt["wgu"], gt["wd"], gt["toff"], o["dab"], o["dx"],
-                          o["dwgu"], o["dwd"], ws)
+@pytest.mark.parametrize("E,d,f,counts", CASES)
+def test_grouped_gemm_kinds(E, d, f, counts, dtype):
+    L, t, gt, rows, ws, o = _setup(E, d, f, counts, dtype)
+    L.moe_grouped_ffn_fwd(gt["x"], gt["wgu"], gt["wd"], gt["toff"], gt["off"], o["ab"], o["h"], o["y"], ws)
+    L.moe_grouped_ffn_bwd(gt["dy"], gt["x"], o["ab"], o["h"], gt["wgu"], gt["wd"], gt["toff"], gt["off"], o["dab"],
+                          o["dx"], o["dwgu"], o["dwd"], ws)
     torch.cuda.synchronize()
     assert L.moe_read_status(ws) == 0
     c = {k: v.double().cpu() for k, v in o.items()}
