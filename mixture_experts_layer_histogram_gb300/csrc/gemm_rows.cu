@@ -14,9 +14,14 @@
 // tiles of one expert, so an expert with an odd number of 128-row tiles computes a discarded tile,
 // and every expert computes its padding up to a multiple of 128 rows. With the weights as A (256
 // output features per pair, 128 per CTA) and the tokens as B, a tile's token count is the MMA's N,
-// which may be any multiple of 16 up to 256. Expert e's c_e rows are split into ceil(c_e / 256)
-// tiles of nearly equal size in multiples of 32 tokens, so the pair computes at most 31 rows past
-// an expert's last token: no discarded tile, no padding beyond the next multiple of 32.
+// which may be any multiple of 16 up to 256. Expert e's c_e rows fill ceil(c_e / 256) tiles: full
+// ones of 256 tokens, then the rest rounded up to a multiple of 32, so the pair computes at most 31
+// rows past an expert's last token: no discarded tile, no padding beyond the next multiple of 32.
+// The tile count is the same as with tokens as A (ceil(ceil(c_e / 128) / 2) = ceil(c_e / 256)
+// pairs), and a tile's time is set mostly by its ring stages (one per 128 of K), not by its N, so
+// the gain is the tensor work (and power) of the rows no longer computed, plus a cheaper epilogue.
+// Every tile loads full 128-row token boxes: loading only the rows a short tile uses took more,
+// smaller TMA requests and was slower.
 //
 // The accumulator is then transposed relative to the output: TMEM lane = output feature, TMEM
 // column = token. The epilogue reads it with tcgen05.ld.16x256b, whose register layout is that of
@@ -89,8 +94,8 @@ struct Params {
   int64_t ld1;
 };
 
-// Tile = (expert e, token tile i, feature tile ft). Expert e's c rows are 32-token units
-// u = ceil(c / 32), split over n = ceil(u / 8) token tiles; the first u % n tiles take one unit more.
+// Tile = (expert e, token tile i, feature tile ft). Expert e's c rows fill n = ceil(c / 256) token
+// tiles: n - 1 full ones of 256 tokens, then the rest rounded up to a multiple of 32.
 struct Tile {
   int e, ft;
   int start;      // first grouped row of the tile
@@ -111,13 +116,11 @@ __device__ __forceinline__ Tile decode(int tile, const Params &p, const int *tto
   t.e = lo;
   const int i = gt - ttoff[lo];
   const int c = p.offsets[lo + 1] - p.offsets[lo];
-  const int u = (c + 31) >> 5;
-  const int n = (u + 7) >> 3;
-  const int q = u / n, r = u - q * n;
-  t.nt = 32 * (q + (i < r ? 1 : 0));
-  const int base = p.tile_offsets[lo] * 128;
-  t.start = base + 32 * (i * q + (i < r ? i : r));
-  t.zero_end = (i == n - 1) ? p.tile_offsets[lo + 1] * 128 : t.start + t.nt;
+  const int n = (c + NT_MAX - 1) / NT_MAX;
+  const bool last = i == n - 1;
+  t.nt = last ? ((c - NT_MAX * i + 31) & ~31) : NT_MAX;
+  t.start = p.tile_offsets[lo] * 128 + NT_MAX * i;
+  t.zero_end = last ? p.tile_offsets[lo + 1] * 128 : t.start + t.nt;
   return t;
 }
 

@@ -1,33 +1,26 @@
-// Grouped GEMM over every expert's SwiGLU FFN on the 5th-generation tensor cores (sm_103a).
+// Grouped GEMMs on the 5th-generation tensor cores (sm_103a) whose reduction runs over the rows of
+// a group: the expert weight gradients, and the router's backward.
 //
 // "Scalable Pretraining of Large MoE LMs on Aurora", brief, section 核心方法: the experts'
-// computation is merged into one grouped GEMM; summary page, section 关键设计: with optimised
-// matrix multiplication and activation. Here one persistent, warp-specialised kernel per GEMM, in
-// two forms. The CTA-pair kernel further down (tcgen05.mma.cta_group::2 on a cluster of two CTAs,
-// 256 x 256 tiles, three 128-deep ring stages, DH five 64-deep ones) runs every weight gradient,
-// and the row-grouped kinds once the experts average at least 4 row tiles. The single-CTA kernel
-// described here runs smaller problems and the router's kinds:
+// computation is merged into one grouped GEMM, and (sections 为什么值得记录 / 关键结果) the module is
+// measured on the forward-backward pass. The kinds whose output rows are grouped tokens (GATEUP,
+// DOWN, DH, DGRAD) live in gemm_rows.cu; this file holds the rest, in two persistent,
+// warp-specialised kernels:
+//   WGRAD   dW[e] = act1_e^T act2_e over expert e's rows (A and B read MN-major, K = the expert's
+//           padded row count; experts without rows get zero gradients without touching TMEM), on
+//           the CTA-pair kernel (tcgen05.mma.cta_group::2, 256 x 256 tiles, the pairs run along the
+//           weight rows, three 128-deep ring stages)
+//   RDX     dx (+)= dL Wr (B read MN-major; the epilogue adds the previous dx when asked), and
+//   RDW     fp32 partial dWr = dL_g^T x_g over token range g (A and B MN-major), plain fp32 stores,
+//           the router backward's two kinds, on the single-CTA kernel (one "group" = all tokens for
+//           RDX, one token range per group for RDW):
 //
-//   warp 0      TMA producer: 128B-swizzled tiles of A and B into a 4-stage shared-memory ring
+//   warp 0      TMA producer: 128B-swizzled tiles of A and B into a shared-memory ring
 //   warp 1      allocates the 512 TMEM columns, issues tcgen05.mma (one thread), commits to barriers
 //   warps 2..9  epilogue: tcgen05.ld of the fp32 accumulator (double-buffered in TMEM, 2 x 256
-//               columns) -> fused SwiGLU / SwiGLU-backward / plain -> bf16 -> global; two warps
-//               share each 32-lane TMEM quarter and take one half of the tile's columns each
+//               columns) -> bf16 or fp32 -> global; two warps share each 32-lane TMEM quarter and
+//               take one half of the tile's columns each
 //
-// Tile 128 x 256 x 64 (bf16 in, fp32 accumulate). Every expert's row group is padded to 128 rows,
-// so every tile belongs to one expert and is full; the tile scheduler walks the flattened tile
-// list with a static stride of gridDim.x and finds the expert of a row tile by binary search over
-// tile_offsets. Five kinds share the kernel:
-//   GATEUP  [a | b] = x_perm Wgu[e]^T  (B = 128 gate rows + the matching 128 up rows), epilogue
-//           writes a, b and h = silu(a) * b
-//   DOWN    y = h Wd[e]^T
-//   DH      dh = dy Wd[e]  (B read MN-major), epilogue reads a, b and writes da, db
-//   DGRAD   dx = dab Wgu[e] (B read MN-major)
-//   WGRAD   dW[e] = act1_e^T act2_e over expert e's rows (A and B read MN-major, K = rows of e)
-// and two kinds of the router's backward (single-CTA kernel only; one "group" = all tokens for
-// RDX, one token range per group for RDW):
-//   RDX     dx (+)= dL Wr   (B read MN-major; the epilogue adds the previous dx when asked)
-//   RDW     fp32 partial dWr = dL_g^T x_g over token range g (A and B MN-major), plain fp32 stores
 // Every wait is bounded (0.2 s); on timeout the kernel records MOE_ERR_DEVICE_TIMEOUT in the
 // workspace status word, lets in-flight copies and MMAs land, frees TMEM and returns.
 #include <cuda.h>
@@ -47,15 +40,15 @@ constexpr int EPI_WARPS = 8;                // two warps per TMEM lane quarter, 
 constexpr int EPI_THREADS = EPI_WARPS * 32;
 constexpr int THREADS = 64 + EPI_THREADS;
 constexpr int TMEM_COLS = 2 * BN;           // two fp32 accumulators of 128 lanes x 256 columns
-constexpr int MAX_E = MOE_MAX_EXPERTS;
 constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 32 * 32 * 2 * 2 * EPI_WARPS + 1024 + 256;
 
-enum Kind { GATEUP = 0, DOWN = 1, DH = 2, DGRAD = 3, WGRAD = 4, RDX = 5, RDW = 6 };
+// (the values name the kernel instantiations; the row-grouped kinds 0..3 are in gemm_rows.cu)
+enum Kind { WGRAD = 4, RDX = 5, RDW = 6 };
 // kinds whose tiles reduce over the rows of one group (A and B read MN-major)
 __host__ __device__ constexpr bool row_reduce(int kind) { return kind == WGRAD || kind == RDW; }
-// 16-byte vectors an epilogue thread loads before its accumulator is ready: DH the first chunk of
-// a and b, RDX its row's whole addend (128 columns)
-__host__ __device__ constexpr int pre_count(int kind) { return kind == RDX ? 16 : 8; }
+// 16-byte vectors an epilogue thread of RDX loads before its accumulator is ready: its row's whole
+// addend (128 columns)
+constexpr int PRE = 16;
 
 struct Params {
   const int32_t *tile_offsets;
@@ -63,12 +56,9 @@ struct Params {
   int E, d, f;
   int n_tiles;        // output tiles along N
   int m_tiles;        // WGRAD: output tiles along M' per expert
-  int num_kb;         // row-grouped kinds: K / BK
-  int b_rows_e;       // rows of the weight's 2D view per expert
+  int num_kb;         // RDX: K / BK
   __nv_bfloat16 *out0;
   int64_t ld0;
-  __nv_bfloat16 *out1;
-  int64_t ld1;
   const __nv_bfloat16 *aux;
   int64_t ld_aux;
   int64_t out_e_stride;
@@ -86,10 +76,10 @@ __host__ __device__ constexpr uint32_t idesc_bf16(bool a_mn, bool b_mn) {
 // ----------------------------------------------------------------------------- scheduling ------
 struct Tile {
   int e;       // expert
-  int m0;      // first grouped row (row-grouped kinds) or first row of dW[e] (WGRAD)
-  int n0;      // first output column (GATEUP: first gate column)
+  int m0;      // RDX: first token row; WGRAD, RDW: first row of the weight gradient
+  int n0;      // first output column
   int kb;      // number of BK blocks
-  int krow0;   // WGRAD: first grouped row of expert e
+  int krow0;   // WGRAD, RDW: first grouped row of the group
 };
 
 template <int KIND>
@@ -114,7 +104,7 @@ __device__ __forceinline__ Tile decode(int tile, const Params &p, const int *tof
     }
     t.e = lo;
     t.m0 = rt * BM;
-    t.n0 = nt * (KIND == GATEUP ? BN / 2 : BN);
+    t.n0 = nt * BN;
     t.kb = p.num_kb;
     t.krow0 = 0;
   }
@@ -163,72 +153,14 @@ struct EpiStore {
   }
 };
 
-// Columns [c0, c0 + cols) of the accumulator (GATEUP: of each half) for the warp's 32 rows; `row`
-// is this thread's row in the tile, `yrow` the global row (in the output map) of the warp's first row.
+// Columns [c0, c0 + BN / 2) of the accumulator for the warp's 32 rows; `row` is this thread's row
+// in the tile, `yrow` the global row (in the output map) of the warp's first row.
 template <int KIND>
 __device__ __forceinline__ void epilogue_tile(const Tile &t, const Params &p, uint32_t tbase, int row, int yrow, int c0,
-                                              const uint4 (&pre)[pre_count(KIND)], EpiStore &es, const CUtensorMap *mc0,
-                                              const CUtensorMap *mc1) {
+                                              const uint4 (&pre)[PRE], EpiStore &es, const CUtensorMap *mc0) {
   float v[32];
   uint32_t r[32];
-  if (KIND == GATEUP) {
-#pragma unroll 1
-    for (int c = c0; c < c0 + BN / 4; c += 32) {
-      uint32_t rb[32];
-      tmem_ld32(tbase + c, r);
-      tmem_ld32(tbase + BN / 2 + c, rb);
-      tmem_ld_wait();
-      float hv[32], bv[32];
-#pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        float a = __uint_as_float(r[i]), b = __uint_as_float(rb[i]);
-        v[i] = a;
-        bv[i] = b;
-        hv[i] = a * sigmoidf_(a) * b;
-      }
-      es.put(mc0, t.n0 + c, yrow, v);           // a  -> ab[:, n0 + c]
-      es.put(mc0, p.f + t.n0 + c, yrow, bv);    // b  -> ab[:, f + n0 + c]
-      es.put(mc1, t.n0 + c, yrow, hv);          // h
-    }
-  } else if (KIND == DH) {
-    // a and b of the current 32 columns arrive one chunk ahead (the first chunk was loaded
-    // before the accumulator was ready): the loads' latency overlaps the previous chunk's work.
-    const __nv_bfloat16 *abrow = p.aux + (int64_t)(t.m0 + row) * p.ld_aux;
-    uint4 cur[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) cur[i] = pre[i];
-#pragma unroll 1
-    for (int c = c0; c < c0 + BN / 2; c += 32) {
-      uint4 nxt[8];
-      if (c + 32 < c0 + BN / 2) {
-        const uint4 *qa = reinterpret_cast<const uint4 *>(abrow + t.n0 + c + 32);
-        const uint4 *qb = reinterpret_cast<const uint4 *>(abrow + p.f + t.n0 + c + 32);
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          nxt[i] = qa[i];
-          nxt[4 + i] = qb[i];
-        }
-      }
-      tmem_ld32(tbase + c, r);
-      float av[32], bv[32], db[32];
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        unpack_bf16x8(cur[i], av + 8 * i);
-        unpack_bf16x8(cur[4 + i], bv + 8 * i);
-      }
-      tmem_ld_wait();
-#pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        const float dh = __uint_as_float(r[i]), a = av[i], s = sigmoidf_(a);
-        v[i] = dh * bv[i] * s * (1.0f + a * (1.0f - s));
-        db[i] = dh * a * s;
-      }
-      es.put(mc0, t.n0 + c, yrow, v);           // da -> dab[:, n0 + c]
-      es.put(mc0, p.f + t.n0 + c, yrow, db);    // db -> dab[:, f + n0 + c]
-#pragma unroll
-      for (int i = 0; i < 8; ++i) cur[i] = nxt[i];
-    }
-  } else if (KIND == RDW) {
+  if (KIND == RDW) {
     // fp32 partial of token range t.e; rows are experts, stored for the first rows_valid only
     const int er = t.m0 + row;
     float *dst = p.outf + ((int64_t)t.e * p.rows_valid + er) * p.ldf + t.n0;
@@ -268,7 +200,7 @@ __device__ __forceinline__ void epilogue_tile(const Tile &t, const Params &p, ui
       if (add) {
         float av[32];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) unpack_bf16x8(pre[(4 * cc + i) % pre_count(KIND)], av + 8 * i);
+        for (int i = 0; i < 4; ++i) unpack_bf16x8(pre[4 * cc + i], av + 8 * i);
 #pragma unroll
         for (int i = 0; i < 32; ++i) v[i] += av[i];
       }
@@ -287,9 +219,10 @@ __device__ __forceinline__ int epi_yrow(const Tile &t, const Params &p, int quar
 template <int KIND>
 __global__ void __launch_bounds__(THREADS, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                   const __grid_constant__ CUtensorMap tmC0, const __grid_constant__ CUtensorMap tmC1, const Params p) {
+                   const __grid_constant__ CUtensorMap tmC0, const Params p) {
+  static_assert(KIND == RDX || KIND == RDW, "the single-CTA kernel runs the router's kinds");
   constexpr bool A_MN = row_reduce(KIND);
-  constexpr bool B_MN = (KIND == DH || KIND == DGRAD || KIND == RDX || row_reduce(KIND));
+  constexpr bool B_MN = true;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t *epi_smem = smem + STAGES * STAGE_BYTES;
@@ -350,19 +283,11 @@ __global__ void __launch_bounds__(THREADS, 1)
         mbar_expect_tx(fb, STAGE_BYTES);
         issued |= 1u << stage;
         const int kx = kb * BK;
-        if (KIND == GATEUP) {
-          tma_load_2d(sA, &tmA, kx, t.m0, fb);
-          tma_load_2d(sB, &tmB, kx, t.e * p.b_rows_e + t.n0, fb);
-          tma_load_2d(sB + B_BYTES / 2, &tmB, kx, t.e * p.b_rows_e + p.f + t.n0, fb);
-        } else if (KIND == DOWN) {
-          tma_load_2d(sA, &tmA, kx, t.m0, fb);
-          tma_load_2d(sB, &tmB, kx, t.e * p.b_rows_e + t.n0, fb);
-          tma_load_2d(sB + B_BYTES / 2, &tmB, kx, t.e * p.b_rows_e + t.n0 + BN / 2, fb);
-        } else if (KIND == DH || KIND == DGRAD || KIND == RDX) {
+        if (KIND == RDX) {   // K-major A (dL rows), MN-major B (Wr; rows past E read as zero)
           tma_load_2d(sA, &tmA, kx, t.m0, fb);
 #pragma unroll
-          for (int q = 0; q < BN / 64; ++q) tma_load_2d(sB + q * 8192, &tmB, t.n0 + 64 * q, t.e * p.b_rows_e + kx, fb);
-        } else {   // WGRAD, RDW
+          for (int q = 0; q < BN / 64; ++q) tma_load_2d(sB + q * 8192, &tmB, t.n0 + 64 * q, kx, fb);
+        } else {   // RDW
 #pragma unroll
           for (int q = 0; q < BM / 64; ++q) tma_load_2d(sA + q * 8192, &tmA, t.m0 + 64 * q, t.krow0 + kx, fb);
 #pragma unroll
@@ -423,48 +348,33 @@ __global__ void __launch_bounds__(THREADS, 1)
     const int quarter = warp & 3;                       // TMEM lanes this warp may access: 32 * quarter ...
     const int half = (warp - 2) >> 2;                   // which half of the tile's columns
     const int row_in_tile = quarter * 32 + lane;
-    const int c0 = half * (KIND == GATEUP ? BN / 4 : BN / 2);
+    const int c0 = half * (BN / 2);
     EpiStore es{smem_u32(epi_smem) + (uint32_t)(warp - 2) * 2 * EPI_BUF_BYTES, 0, lane};
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
       const Tile t = decode<KIND>(tile, p, toff);
-      if (t.kb == 0) {   // a group with no rows: its gradient (partial) is zero
-        if (KIND == RDW) {
-          const int er = t.m0 + row_in_tile;
-          if (er < p.rows_valid) {
-            float *dst = p.outf + ((int64_t)t.e * p.rows_valid + er) * p.ldf + t.n0 + c0;
-            for (int i = 0; i < BN / 2; i += 4)
-              if (t.n0 + c0 + i < p.d) *reinterpret_cast<float4 *>(dst + i) = make_float4(0.f, 0.f, 0.f, 0.f);
-          }
-        } else {
-          __nv_bfloat16 *dst =
-              p.out0 + (int64_t)t.e * p.out_e_stride + (int64_t)(t.m0 + row_in_tile) * p.ld0 + t.n0 + c0;
-          uint4 *q = reinterpret_cast<uint4 *>(dst);
-          for (int i = 0; i < BN / 16; ++i) q[i] = make_uint4(0, 0, 0, 0);
+      if (t.kb == 0) {   // RDW, a token range with no rows: its partial is zero
+        const int er = t.m0 + row_in_tile;
+        if (er < p.rows_valid) {
+          float *dst = p.outf + ((int64_t)t.e * p.rows_valid + er) * p.ldf + t.n0 + c0;
+          for (int i = 0; i < BN / 2; i += 4)
+            if (t.n0 + c0 + i < p.d) *reinterpret_cast<float4 *>(dst + i) = make_float4(0.f, 0.f, 0.f, 0.f);
         }
         continue;
       }
-      uint4 pre[pre_count(KIND)];
-      if (KIND == DH) {   // first chunk of a, b: independent of the MMA, load before waiting
-        const __nv_bfloat16 *abrow = p.aux + (int64_t)(t.m0 + row_in_tile) * p.ld_aux + t.n0 + c0;
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          pre[i] = reinterpret_cast<const uint4 *>(abrow)[i];
-          pre[4 + i] = reinterpret_cast<const uint4 *>(abrow + p.f)[i];
-        }
-      }
-      if (KIND == RDX && p.aux != nullptr) {   // the addend row: independent of the MMA as well
+      uint4 pre[PRE];
+      if (KIND == RDX && p.aux != nullptr) {   // the addend row: independent of the MMA, load before waiting
         const bool live = t.m0 + row_in_tile < p.rows_valid;
         const __nv_bfloat16 *arow = p.aux + (int64_t)(live ? t.m0 + row_in_tile : 0) * p.ld_aux + t.n0 + c0;
 #pragma unroll
-        for (int i = 0; i < pre_count(KIND); ++i)
+        for (int i = 0; i < PRE; ++i)
           pre[i] = (live && t.n0 + c0 + 8 * i < p.d) ? reinterpret_cast<const uint4 *>(arow)[i] : make_uint4(0, 0, 0, 0);
       }
       if (!mbar_wait(tfull_bar(acc), acc_phase, abort_flag, p.hdr, 4)) break;
       tc_fence_after();
       const uint32_t tbase = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * BN);
-      epilogue_tile<KIND>(t, p, tbase, row_in_tile, epi_yrow<KIND>(t, p, quarter), c0, pre, es, &tmC0, &tmC1);
+      epilogue_tile<KIND>(t, p, tbase, row_in_tile, epi_yrow<KIND>(t, p, quarter), c0, pre, es, &tmC0);
       tc_fence_before();
       mbar_arrive(tempty_bar(acc));
       acc ^= 1;
@@ -483,92 +393,61 @@ __global__ void __launch_bounds__(THREADS, 1)
 }
 
 // ----------------------------------------------------------------------------- CTA-pair kernel --
-// A cluster of two CTAs (one TPC) computes a 256 x 256 tile with tcgen05.mma.cta_group::2: CTA r
-// holds rows [128 r, 128 r + 128) of A and half r of B (N rows [128 r, 128 r + 128)) in its own
-// shared memory, and receives its 128 rows x 256 columns of the accumulator in its own TMEM. Each
-// SM therefore loads 32 KB per 64-deep k-block instead of 48 KB for the same MMA work. The leader
-// (rank 0) issues the MMAs; both CTAs' TMA loads complete on the leader's full barrier; the MMA
-// commits multicast to both CTAs' empty / accumulator-full barriers; both epilogues arrive on the
-// leader's accumulator-empty barrier. Row-grouped kinds pair two consecutive row tiles of one
-// expert; when an expert has an odd number of row tiles, the second CTA of its last pair computes
-// rows past the expert and discards them.
-// Per-kind ring. Each stage costs the MMA thread one full-barrier wait and one commit, and the
-// producer one empty-barrier wait. With 64-deep stages those hand-offs held the tensor pipe to
-// 72-77% of its rate whether or not any operand was loaded, so every kind runs 128-deep stages
-// (three of 64 KB). The exception is DH: its epilogue brings the saved a, b blocks in by TMA, into two 4 KB
-// buffers per epilogue warp (64 KB, filled two 32-column chunks ahead), which leaves room for five
-// 64-deep stages only; two 128-deep stages were slower.
-constexpr int DH_BUF_BYTES = 2 * EPI_BUF_BYTES;   // a block + b block of one chunk
-template <int KIND> struct PairCfg {
-  static constexpr int BKP = KIND == DH ? 64 : 128;       // k depth of one ring stage (a multiple of 64)
-  static constexpr int KA = BKP / 64;                     // 128-byte swizzle atoms along k per stage
+// The weight gradients on a cluster of two CTAs (one TPC): tcgen05.mma.cta_group::2 computes a
+// 256 x 256 tile of dW[e]; CTA r holds rows [128 r, 128 r + 128) of A (weight rows m0 + 128 r) and
+// half r of B (N rows [128 r, 128 r + 128)) in its own shared memory, and receives its 128 rows x
+// 256 columns of the accumulator in its own TMEM. Each SM therefore loads 32 KB per 64-deep k-block
+// instead of 48 KB for the same MMA work. The leader (rank 0) issues the MMAs; both CTAs' TMA loads
+// complete on the leader's full barrier; the MMA commits multicast to both CTAs' empty /
+// accumulator-full barriers; both epilogues arrive on the leader's accumulator-empty barrier. The
+// pairs run along the weight rows, so no tile is discarded; K is the expert's padded row count.
+// Each ring stage costs the MMA thread one full-barrier wait and one commit, and the producer one
+// empty-barrier wait; with 64-deep stages those hand-offs held the tensor pipe to 72-77% of its
+// rate whether or not any operand was loaded, so the ring has three 128-deep stages of 64 KB.
+struct PairCfg {
+  static constexpr int BKP = 128;                         // k depth of one ring stage
   static constexpr int A_BYTES = BM * BKP * 2;            // this CTA's 128 rows of A
   static constexpr int B_BYTES = (BN / 2) * BKP * 2;      // this CTA's half of B
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-  static constexpr int STAGES = KIND == DH ? 5 : 3;
-  static constexpr int EPI_BYTES = KIND == DH ? EPI_WARPS * 2 * DH_BUF_BYTES : EPI_STAGE_BYTES;
-  static constexpr int NBARS = 2 * STAGES + 5 + (KIND == DH ? 2 * EPI_WARPS : 0);
-  static constexpr int SMEM = STAGES * STAGE_BYTES + EPI_BYTES + 1024 + 8 * NBARS + 16 + (MAX_E + 1) * 4;
+  static constexpr int STAGES = 3;
+  static constexpr int EPI_BYTES = EPI_STAGE_BYTES;
+  static constexpr int NBARS = 2 * STAGES + 5;
+  static constexpr int SMEM = STAGES * STAGE_BYTES + EPI_BYTES + 1024 + 8 * NBARS + 16;
   static_assert(SMEM <= 232448, "pair kernel shared memory exceeds 227 KB");
 };
 
-// Instruction descriptor for the pair MMA: M = 256 (128 rows per CTA), N = 256.
-__host__ __device__ constexpr uint32_t idesc_bf16_pair(bool a_mn, bool b_mn) {
-  return (1u << 4) | (1u << 7) | (1u << 10) | ((a_mn ? 1u : 0u) << 15) | ((b_mn ? 1u : 0u) << 16) |
-         ((uint32_t)(BN >> 3) << 17) | ((uint32_t)((2 * BM) >> 4) << 24);
+// Instruction descriptor for the pair MMA: M = 256 (128 rows per CTA), N = 256, A and B MN-major.
+__host__ __device__ constexpr uint32_t idesc_bf16_pair_mn() {
+  return (1u << 4) | (1u << 7) | (1u << 10) | (1u << 15) | (1u << 16) | ((uint32_t)(BN >> 3) << 17) |
+         ((uint32_t)((2 * BM) >> 4) << 24);
 }
 
-// The pair tile as seen from CTA `rank`; valid = false when this CTA's row tile lies past its expert.
-template <int KIND>
-__device__ __forceinline__ Tile decode_pair(int tile, const Params &p, const int *toff, const int *ptoff, int rank,
-                                            bool &valid) {
+// The weight-gradient tile (expert e, row pair, N tile) as seen from CTA `rank`.
+__device__ __forceinline__ Tile decode_wgrad(int tile, const Params &p, const int *toff, int rank) {
   Tile t;
-  valid = true;
-  if (KIND == WGRAD) {
-    const int per = (p.m_tiles / 2) * p.n_tiles;
-    t.e = tile / per;
-    const int r = tile - t.e * per;
-    t.m0 = (r / p.n_tiles) * (2 * BM) + rank * BM;
-    t.n0 = (r % p.n_tiles) * BN;
-    t.krow0 = toff[t.e] * BM;
-    t.kb = (toff[t.e + 1] - toff[t.e]) * (BM / PairCfg<KIND>::BKP);
-  } else {
-    const int pr = tile / p.n_tiles;
-    const int nt = tile - pr * p.n_tiles;
-    int lo = 0, hi = p.E - 1;   // last expert whose first pair row is <= pr
-    while (lo < hi) {
-      int mid = (lo + hi + 1) >> 1;
-      if (ptoff[mid] <= pr) lo = mid;
-      else hi = mid - 1;
-    }
-    t.e = lo;
-    const int rt = toff[t.e] + 2 * (pr - ptoff[t.e]) + rank;
-    valid = rt < toff[t.e + 1];
-    t.m0 = rt * BM;
-    t.n0 = nt * (KIND == GATEUP ? BN / 2 : BN);
-    t.kb = p.num_kb / PairCfg<KIND>::KA;
-    t.krow0 = 0;
-  }
+  const int per = (p.m_tiles / 2) * p.n_tiles;
+  t.e = tile / per;
+  const int r = tile - t.e * per;
+  t.m0 = (r / p.n_tiles) * (2 * BM) + rank * BM;
+  t.n0 = (r % p.n_tiles) * BN;
+  t.krow0 = toff[t.e] * BM;
+  t.kb = (toff[t.e + 1] - toff[t.e]) * (BM / PairCfg::BKP);
   return t;
 }
 
-template <int KIND>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     tc_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                   const __grid_constant__ CUtensorMap tmC0, const __grid_constant__ CUtensorMap tmC1, const Params p) {
-  constexpr bool A_MN = (KIND == WGRAD);
-  constexpr bool B_MN = (KIND == DH || KIND == DGRAD || KIND == WGRAD);
-  using Cfg = PairCfg<KIND>;
+                   const __grid_constant__ CUtensorMap tmC0, const Params p) {
+  using Cfg = PairCfg;
   constexpr int PS = Cfg::STAGES;
-  constexpr int P_BK = Cfg::BKP, P_KA = Cfg::KA;
+  constexpr int P_BK = Cfg::BKP;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t *epi_smem = smem + PS * Cfg::STAGE_BYTES;
-  uint64_t *bars = reinterpret_cast<uint64_t *>(epi_smem + PairCfg<KIND>::EPI_BYTES);
-  // bars: full[PS], empty[PS], tfull[2], tempty[2], mma_done, (DH) two load barriers per epilogue warp
-  uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(bars + PairCfg<KIND>::NBARS);
+  uint64_t *bars = reinterpret_cast<uint64_t *>(epi_smem + Cfg::EPI_BYTES);
+  // bars: full[PS], empty[PS], tfull[2], tempty[2], mma_done
+  uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(bars + Cfg::NBARS);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_holder + 1);
-  int *ptoff = reinterpret_cast<int *>(tmem_holder + 4);
   const int *toff = p.tile_offsets;   // read through L1; shared memory goes to the ring
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -592,37 +471,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
       mbar_init(tempty_bar(a), 2 * EPI_WARPS);   // one arrival per epilogue warp of both CTAs
     }
     mbar_init(mma_done_bar, 1);
-    if (KIND == DH)
-      for (int i = 0; i < 2 * EPI_WARPS; ++i) mbar_init(bar0 + 8u * (2 * PS + 5 + i), 1);
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmA)) : "memory");
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmB)) : "memory");
   }
   __syncthreads();
-  if (KIND != WGRAD && warp == 0) {   // ptoff = exclusive scan of ceil(row tiles / 2) per expert
-    int c[8], sum = 0;
-#pragma unroll
-    for (int q = 0; q < 8; ++q) {
-      const int e = lane * 8 + q;
-      c[q] = e < p.E ? (toff[e + 1] - toff[e] + 1) / 2 : 0;
-      sum += c[q];
-    }
-    int incl = sum;
-#pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-      const int v = __shfl_up_sync(0xffffffffu, incl, off);
-      if (lane >= off) incl += v;
-    }
-    int run = incl - sum;
-#pragma unroll
-    for (int q = 0; q < 8; ++q) {
-      const int e = lane * 8 + q;
-      if (e < p.E) ptoff[e] = run;
-      run += c[q];
-    }
-    if (lane == 31) ptoff[p.E] = incl;
-  }
   if (warp == 1) {   // collective TMEM allocation by one warp of each CTA of the pair
     asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_holder)),
                  "r"((uint32_t)TMEM_COLS)
@@ -634,60 +488,39 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
   tc_fence_after();
   const uint32_t tmem_base = *tmem_holder;
 
-  const int num_tiles = (KIND == WGRAD) ? p.E * (p.m_tiles / 2) * p.n_tiles : ptoff[p.E] * p.n_tiles;
+  const int num_tiles = p.E * (p.m_tiles / 2) * p.n_tiles;
   const int cluster_id = blockIdx.x >> 1, num_clusters = gridDim.x >> 1;
 
   if (warp == 0 && lane == 0) {
     // ------------------------------------------------------------------ TMA producer (both CTAs)
-    // Boxes of k-block kb of tile t for this CTA, loaded into ring stage (sA, sB).
-    auto boxes = [&](const Tile &t, int kb, uint32_t sA, uint32_t sB, uint32_t fb) {
-      auto box = [&](const CUtensorMap *m, int x, int y, uint32_t dst) { tma_load_2d_pair(dst, m, x, y, fb); };
-      const int kx = kb * P_BK;
-      const int bn = t.n0 + (int)rank * (BN / 2);             // this CTA's half of B
-      if (KIND == GATEUP || KIND == DOWN) {                   // K-major A and B: one 64-wide box per atom
-        const int brow = t.e * p.b_rows_e + (KIND == GATEUP ? (rank ? p.f : 0) + t.n0 : bn);
-#pragma unroll
-        for (int a = 0; a < P_KA; ++a) {
-          box(&tmA, kx + 64 * a, t.m0, sA + a * (BM * 128));
-          box(&tmB, kx + 64 * a, brow, sB + a * ((BN / 2) * 128));
-        }
-      } else if (KIND == DH || KIND == DGRAD) {               // K-major A, MN-major B (64 x P_BK boxes)
-#pragma unroll
-        for (int a = 0; a < P_KA; ++a) box(&tmA, kx + 64 * a, t.m0, sA + a * (BM * 128));
-#pragma unroll
-        for (int q = 0; q < 2; ++q) box(&tmB, bn + 64 * q, t.e * p.b_rows_e + kx, sB + q * (P_BK * 128));
-      } else {   // WGRAD: MN-major A and B
-#pragma unroll
-        for (int q = 0; q < 2; ++q) box(&tmA, t.m0 + 64 * q, t.krow0 + kx, sA + q * (P_BK * 128));
-#pragma unroll
-        for (int q = 0; q < 2; ++q) box(&tmB, bn + 64 * q, t.krow0 + kx, sB + q * (P_BK * 128));
-      }
-    };
     int stage = 0;
     uint32_t phase = 0;
     for (int tile = cluster_id; tile < num_tiles; tile += num_clusters) {
-      bool valid;
-      const Tile t = decode_pair<KIND>(tile, p, toff, ptoff, (int)rank, valid);
+      const Tile t = decode_wgrad(tile, p, toff, (int)rank);
+      const int bn = t.n0 + (int)rank * (BN / 2);   // this CTA's half of B
       bool ok = true;
       for (int kb = 0; kb < t.kb; ++kb) {
         if (!mbar_spin_cluster(empty_bar(stage), phase ^ 1u, abort_flag, p.hdr, 11)) { ok = false; break; }
         const uint32_t sA = sbase + stage * Cfg::STAGE_BYTES, sB = sA + Cfg::A_BYTES;
         const uint32_t fb = mapa_shared(full_bar(stage), 0);   // the leader's full barrier
         if (leader) mbar_expect_tx(full_bar(stage), 2 * Cfg::STAGE_BYTES);
-        boxes(t, kb, sA, sB, fb);
+        const int ky = t.krow0 + kb * P_BK;
+#pragma unroll
+        for (int q = 0; q < 2; ++q) tma_load_2d_pair(sA + q * (P_BK * 128), &tmA, t.m0 + 64 * q, ky, fb);
+#pragma unroll
+        for (int q = 0; q < 2; ++q) tma_load_2d_pair(sB + q * (P_BK * 128), &tmB, bn + 64 * q, ky, fb);
         if (++stage == PS) { stage = 0; phase ^= 1u; }
       }
       if (!ok) break;
     }
   } else if (warp == 1 && lane == 0 && leader) {
     // ------------------------------------------------------------------ MMA issuer (leader only)
-    constexpr uint32_t idesc = idesc_bf16_pair(A_MN, B_MN);
+    constexpr uint32_t idesc = idesc_bf16_pair_mn();
     int stage = 0, acc = 0;
     uint32_t phase = 0, acc_phase = 0;
     bool issued_any = false;
     for (int tile = cluster_id; tile < num_tiles; tile += num_clusters) {
-      bool valid;
-      const Tile t = decode_pair<KIND>(tile, p, toff, ptoff, 0, valid);
+      const Tile t = decode_wgrad(tile, p, toff, 0);
       if (t.kb == 0) continue;
       if (!mbar_wait_cluster(tempty_bar(acc), acc_phase ^ 1u, abort_flag, p.hdr, 12)) break;
       tc_fence_after();
@@ -699,11 +532,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
         const uint32_t sA = sbase + stage * Cfg::STAGE_BYTES, sB = sA + Cfg::A_BYTES;
 #pragma unroll
         for (int kk = 0; kk < P_BK / 16; ++kk) {
-          // K-major: atom kk/4 (128 rows x 128 B each), 32 B per 16-deep step inside the atom.
-          // MN-major: 2048 B per 16 k-rows; MN blocks of 64 are P_BK * 128 B apart.
-          const uint32_t koff = (uint32_t)((kk >> 2) * (BM * 128) + (kk & 3) * 32);
-          const uint64_t ad = A_MN ? sdesc(sA + kk * 2048, P_BK * 128, 1024) : sdesc(sA + koff, 16, 1024);
-          const uint64_t bd = B_MN ? sdesc(sB + kk * 2048, P_BK * 128, 1024) : sdesc(sB + koff, 16, 1024);
+          // MN-major: 2048 B per 16 k-rows; the two 64-wide MN blocks are P_BK * 128 B apart.
+          const uint64_t ad = sdesc(sA + kk * 2048, P_BK * 128, 1024);
+          const uint64_t bd = sdesc(sB + kk * 2048, P_BK * 128, 1024);
           mma_bf16_pair(d_tmem, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
         }
         issued_any = true;
@@ -720,137 +551,29 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
       const uint64_t t0 = global_ns();
       while (!mbar_try_wait(mma_done_bar, 0) && global_ns() - t0 < kWaitLimitNs) {}
     }
-  } else if (warp >= 2 && KIND == DH) {
-    // ------------------------------------------------------------------ DH epilogue (both CTAs)
-    // Per warp: its 32 rows x one 128-column half of the tile, in four 32-column chunks. The saved
-    // a and b blocks of a chunk arrive by TMA (tmC1 = ab) into one of two 4 KB buffers two chunks
-    // ahead of use (across tiles); da and db are written back in place and stored by TMA (tmC0 = dab).
-    const int quarter = warp & 3;
-    const int half = (warp - 2) >> 2;
-    const int c0 = half * (BN / 2);
-    const uint32_t dbuf = smem_u32(epi_smem) + (uint32_t)(warp - 2) * 2 * DH_BUF_BYTES;
-    const uint32_t lbar = bar0 + 8u * (2 * PS + 5 + 2 * (warp - 2));
-    uint32_t lphase = 0;   // bit b: parity of buffer b's next fill
-    // load cursor: next (tile, chunk) to bring in
-    int ltile = cluster_id, lj = 0;
-    auto issue_load = [&](int bi) {
-      if (ltile >= num_tiles) return;
-      bool lv;
-      const Tile lt = decode_pair<KIND>(ltile, p, toff, ptoff, (int)rank, lv);
-      if (lane == 0) {
-        asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");   // the buffer's last store has read it
-        const uint32_t b = dbuf + (uint32_t)bi * DH_BUF_BYTES, bar = lbar + 8u * bi;
-        const int x = lt.n0 + c0 + 32 * lj, y = lt.m0 + quarter * 32;
-        mbar_expect_tx(bar, DH_BUF_BYTES);
-        tma_load_2d(b, &tmC1, x, y, bar);
-        tma_load_2d(b + EPI_BUF_BYTES, &tmC1, p.f + x, y, bar);
-      }
-      if (++lj == 4) { lj = 0; ltile += num_clusters; }
-    };
-    issue_load(0);
-    issue_load(1);
-    int acc = 0, bi = 0;
-    uint32_t acc_phase = 0;
-    const uint32_t sw = (uint32_t)(lane >> 1) & 3u;
-    for (int tile = cluster_id; tile < num_tiles; tile += num_clusters) {
-      bool valid;
-      const Tile t = decode_pair<KIND>(tile, p, toff, ptoff, (int)rank, valid);
-      if (!mbar_wait_cluster(tfull_bar(acc), acc_phase, abort_flag, p.hdr, 14)) break;
-      tc_fence_after();
-      const uint32_t tbase = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * BN);
-      const int yrow = t.m0 + quarter * 32;
-      bool ok = true;
-#pragma unroll 1
-      for (int j = 0; j < 4; ++j) {
-        const int c = c0 + 32 * j;
-        uint32_t r[32];
-        tmem_ld32(tbase + c, r);
-        if (!mbar_wait_cluster(lbar + 8u * bi, (lphase >> bi) & 1u, abort_flag, p.hdr, 17)) { ok = false; break; }
-        lphase ^= 1u << bi;
-        const uint32_t ra = dbuf + (uint32_t)bi * DH_BUF_BYTES + (uint32_t)lane * 64, rb = ra + EPI_BUF_BYTES;
-        float av[32], bv[32];
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          uint4 qa, qb;
-          const uint32_t off = (uint32_t)(q ^ sw) << 4;
-          asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];" : "=r"(qa.x), "=r"(qa.y), "=r"(qa.z), "=r"(qa.w)
-                       : "r"(ra + off));
-          asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];" : "=r"(qb.x), "=r"(qb.y), "=r"(qb.z), "=r"(qb.w)
-                       : "r"(rb + off));
-          unpack_bf16x8(qa, av + 8 * q);
-          unpack_bf16x8(qb, bv + 8 * q);
-        }
-        tmem_ld_wait();
-        float da[32], db[32];
-#pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          const float dh = __uint_as_float(r[i]), a = av[i], sg = sigmoidf_(a);
-          da[i] = dh * bv[i] * sg * (1.0f + a * (1.0f - sg));
-          db[i] = dh * a * sg;
-        }
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const uint32_t off = (uint32_t)(q ^ sw) << 4;
-          const uint4 qa = pack_bf16x8(da + 8 * q), qb = pack_bf16x8(db + 8 * q);
-          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(ra + off), "r"(qa.x), "r"(qa.y), "r"(qa.z),
-                       "r"(qa.w)
-                       : "memory");
-          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(rb + off), "r"(qb.x), "r"(qb.y), "r"(qb.z),
-                       "r"(qb.w)
-                       : "memory");
-        }
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-        __syncwarp();
-        if (valid && lane == 0) {
-          const uint32_t b = dbuf + (uint32_t)bi * DH_BUF_BYTES;
-          asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
-                           reinterpret_cast<uint64_t>(&tmC0)),
-                       "r"(t.n0 + c), "r"(yrow), "r"(b)
-                       : "memory");
-          asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
-                           reinterpret_cast<uint64_t>(&tmC0)),
-                       "r"(p.f + t.n0 + c), "r"(yrow), "r"(b + EPI_BUF_BYTES)
-                       : "memory");
-          asm volatile("cp.async.bulk.commit_group;" ::: "memory");
-        }
-        issue_load(bi);   // the chunk two ahead reuses this buffer once its store has read it
-        __syncwarp();
-        bi ^= 1;
-      }
-      if (!ok) break;
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive_cluster(mapa_shared(tempty_bar(acc), 0));
-      acc ^= 1;
-      if (acc == 0) acc_phase ^= 1u;
-    }
-    if (lane == 0) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
-    __syncwarp();
   } else if (warp >= 2) {
     // ------------------------------------------------------------------ epilogue (both CTAs)
     const int quarter = warp & 3;
     const int half = (warp - 2) >> 2;
     const int row_in_tile = quarter * 32 + lane;
-    const int c0 = half * (KIND == GATEUP ? BN / 4 : BN / 2);
+    const int c0 = half * (BN / 2);
     EpiStore es{smem_u32(epi_smem) + (uint32_t)(warp - 2) * 2 * EPI_BUF_BYTES, 0, lane};
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int tile = cluster_id; tile < num_tiles; tile += num_clusters) {
-      bool valid;
-      const Tile t = decode_pair<KIND>(tile, p, toff, ptoff, (int)rank, valid);
-      if (t.kb == 0) {   // WGRAD of an expert with no rows: the gradient is zero
+      const Tile t = decode_wgrad(tile, p, toff, (int)rank);
+      if (t.kb == 0) {   // an expert with no rows: its gradient is zero
         __nv_bfloat16 *dst =
             p.out0 + (int64_t)t.e * p.out_e_stride + (int64_t)(t.m0 + row_in_tile) * p.ld0 + t.n0 + c0;
         uint4 *q = reinterpret_cast<uint4 *>(dst);
         for (int i = 0; i < BN / 16; ++i) q[i] = make_uint4(0, 0, 0, 0);
         continue;
       }
-      uint4 pre[pre_count(KIND)];   // unused here: the pair kernel's DH has its own epilogue above
+      uint4 pre[PRE];   // unused by this kind
       if (!mbar_wait_cluster(tfull_bar(acc), acc_phase, abort_flag, p.hdr, 14)) break;
       tc_fence_after();
       const uint32_t tbase = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * BN);
-      if (valid)
-        epilogue_tile<KIND>(t, p, tbase, row_in_tile, epi_yrow<KIND>(t, p, quarter), c0, pre, es, &tmC0, &tmC1);
+      epilogue_tile<WGRAD>(t, p, tbase, row_in_tile, epi_yrow<WGRAD>(t, p, quarter), c0, pre, es, &tmC0);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive_cluster(mapa_shared(tempty_bar(acc), 0));
@@ -871,55 +594,39 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
 }
 
 // ----------------------------------------------------------------------------- host side -------
-// k rows of an MN-major TMA box: one ring stage of the kernel that reads it
-constexpr uint32_t MN_BOX = BK;   // single-CTA kernel
-template <int KIND> constexpr uint32_t pair_mn_box() { return (uint32_t)PairCfg<KIND>::BKP; }
-
-// The pair kernel pairs two row tiles of one expert, so an expert with an odd number of row tiles
-// computes one tile it throws away; with few row tiles per expert the single-CTA kernel wins.
-static bool use_pair(int kind, int64_t rows_max, int E) {
-  if (kind == WGRAD) return true;   // pairs along the weight rows: no waste
-  return rows_max / BM >= 4 * (int64_t)E;
-}
-
-// The single-CTA kernel on a persistent grid of min(SMs, max_tiles) CTAs.
+// The single-CTA kernel (router kinds) on a persistent grid of min(SMs, max_tiles) CTAs.
 template <int KIND>
-static int launch_single(const CUtensorMap &a, const CUtensorMap &b, const CUtensorMap &c0, const CUtensorMap &c1,
-                         const Params &p, int64_t max_tiles, cudaStream_t s) {
+static int launch_single(const CUtensorMap &a, const CUtensorMap &b, const CUtensorMap &c0, const Params &p,
+                         int64_t max_tiles, cudaStream_t s) {
   MOE_TRY_CUDA(cudaFuncSetAttribute(tc_gemm_kernel<KIND>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES));
   int64_t grid = sm_count();
   if (max_tiles < grid) grid = max_tiles;
   if (grid < 1) grid = 1;
-  tc_gemm_kernel<KIND><<<(int)grid, THREADS, SMEM_BYTES, s>>>(a, b, c0, c1, p);
+  tc_gemm_kernel<KIND><<<(int)grid, THREADS, SMEM_BYTES, s>>>(a, b, c0, p);
   MOE_CHECK_LAUNCH();
   return MOE_OK;
 }
 
-// max_tiles / max_pair_tiles: host upper bounds on the tile counts (the exact counts live on the device)
-template <int KIND>
-static int launch(const CUtensorMap &a, const CUtensorMap &b, const CUtensorMap &c0, const CUtensorMap &c1,
-                  const Params &p, int64_t max_tiles, int64_t max_pair_tiles, bool pair, cudaStream_t s) {
-  if (pair) {
-    constexpr int smem = PairCfg<KIND>::SMEM;
-    MOE_TRY_CUDA(cudaFuncSetAttribute(tc_pair_kernel<KIND>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem));
-    // a persistent grid must fit at once: launch only as many pairs as can be co-resident
-    int resident = 0;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)(sm_count() / 2 * 2), 1, 1);
-    cfg.blockDim = dim3(THREADS, 1, 1);
-    cfg.dynamicSmemBytes = smem;
-    if (cudaOccupancyMaxActiveClusters(&resident, tc_pair_kernel<KIND>, &cfg) != cudaSuccess || resident < 1) {
-      (void)cudaGetLastError();
-      resident = sm_count() / 2;
-    }
-    int64_t clusters = resident;
-    if (max_pair_tiles < clusters) clusters = max_pair_tiles;
-    if (clusters < 1) clusters = 1;
-    tc_pair_kernel<KIND><<<(int)(2 * clusters), THREADS, smem, s>>>(a, b, c0, c1, p);
-    MOE_CHECK_LAUNCH();
-    return MOE_OK;
+// The weight-gradient kind on a persistent grid of as many CTA pairs as can be resident at once.
+static int launch_wgrad(const CUtensorMap &a, const CUtensorMap &b, const CUtensorMap &c0, const Params &p,
+                        int64_t max_pair_tiles, cudaStream_t s) {
+  constexpr int smem = PairCfg::SMEM;
+  MOE_TRY_CUDA(cudaFuncSetAttribute(tc_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem));
+  int resident = 0;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(sm_count() / 2 * 2), 1, 1);
+  cfg.blockDim = dim3(THREADS, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  if (cudaOccupancyMaxActiveClusters(&resident, tc_pair_kernel, &cfg) != cudaSuccess || resident < 1) {
+    (void)cudaGetLastError();
+    resident = sm_count() / 2;
   }
-  return launch_single<KIND>(a, b, c0, c1, p, max_tiles, s);
+  int64_t clusters = resident;
+  if (max_pair_tiles < clusters) clusters = max_pair_tiles;
+  if (clusters < 1) clusters = 1;
+  tc_pair_kernel<<<(int)(2 * clusters), THREADS, smem, s>>>(a, b, c0, p);
+  MOE_CHECK_LAUNCH();
+  return MOE_OK;
 }
 
 }  // namespace tc
@@ -960,7 +667,7 @@ int tc_grouped_ffn_bwd(const void *dy, const void *x_perm, const void *ab, const
   // dh = dy Wd[e] (Wd read MN-major), SwiGLU backward epilogue -> dab
   if ((rc = rows_dh(dy, wd, ab, tile_offsets, offsets, E, d, f, rows_max, dab, hdr, s))) return rc;
   // dWd[e] = dy_e^T h_e (the weight-gradient kind runs on the CTA-pair kernel, whose stage depth its maps take)
-  if (!make_map(&mA, dy, rows_max, d, pair_mn_box<WGRAD>()) || !make_map(&mB, h, rows_max, f, pair_mn_box<WGRAD>()) ||
+  if (!make_map(&mA, dy, rows_max, d, PairCfg::BKP) || !make_map(&mB, h, rows_max, f, PairCfg::BKP) ||
       !make_store_map(&mC, dwd, (uint64_t)E * d, f))
     return MOE_ERR_CUDA;
   p.m_tiles = d / BM;
@@ -968,14 +675,12 @@ int tc_grouped_ffn_bwd(const void *dy, const void *x_perm, const void *ab, const
   p.out0 = (__nv_bfloat16 *)dwd;
   p.ld0 = f;
   p.out_e_stride = (int64_t)d * f;
-  if ((rc = launch<WGRAD>(mA, mB, mC, mC, p, (int64_t)E * p.m_tiles * p.n_tiles,
-                          (int64_t)E * (p.m_tiles / 2) * p.n_tiles, true, s)))
+  if ((rc = launch_wgrad(mA, mB, mC, p, (int64_t)E * (p.m_tiles / 2) * p.n_tiles, s)))
     return rc;
   // dx_perm = dab Wgu[e] (Wgu read MN-major)
   if ((rc = rows_dgrad(dab, wgu, tile_offsets, offsets, E, d, f, rows_max, dx, hdr, s))) return rc;
   // dWgu[e] = dab_e^T x_perm_e
-  if (!make_map(&mA, dab, rows_max, 2 * f, pair_mn_box<WGRAD>()) ||
-      !make_map(&mB, x_perm, rows_max, d, pair_mn_box<WGRAD>()) ||
+  if (!make_map(&mA, dab, rows_max, 2 * f, PairCfg::BKP) || !make_map(&mB, x_perm, rows_max, d, PairCfg::BKP) ||
       !make_store_map(&mC, dwgu, (uint64_t)E * 2 * f, d))
     return MOE_ERR_CUDA;
   p.m_tiles = 2 * f / BM;
@@ -983,8 +688,7 @@ int tc_grouped_ffn_bwd(const void *dy, const void *x_perm, const void *ab, const
   p.out0 = (__nv_bfloat16 *)dwgu;
   p.ld0 = d;
   p.out_e_stride = (int64_t)2 * f * d;
-  return launch<WGRAD>(mA, mB, mC, mC, p, (int64_t)E * p.m_tiles * p.n_tiles, (int64_t)E * (p.m_tiles / 2) * p.n_tiles,
-                       true, s);
+  return launch_wgrad(mA, mB, mC, p, (int64_t)E * (p.m_tiles / 2) * p.n_tiles, s);
 }
 
 // Router backward GEMMs (router.cu prepares dl16, the bf16 copy of d_logits [t_pad, ek] with zero
@@ -994,7 +698,7 @@ int tc_router_dx(const void *dl16, int64_t t_pad, int ek, const void *wr, int E,
                  const int32_t *toff, void *dx, bool accumulate, WsHeader *hdr, cudaStream_t s) {
   using namespace tc;
   CUtensorMap mA, mB, mC;
-  if (!make_map(&mA, dl16, t_pad, ek, 128) || !make_map(&mB, wr, E, d, MN_BOX) || !make_store_map(&mC, dx, T, d))
+  if (!make_map(&mA, dl16, t_pad, ek, 128) || !make_map(&mB, wr, E, d, BK) || !make_store_map(&mC, dx, T, d))
     return MOE_ERR_CUDA;
   Params p{};
   p.tile_offsets = toff;
@@ -1003,13 +707,12 @@ int tc_router_dx(const void *dl16, int64_t t_pad, int ek, const void *wr, int E,
   p.d = d;
   p.n_tiles = (d + BN - 1) / BN;
   p.num_kb = ek / BK;
-  p.b_rows_e = 0;
   p.out0 = (__nv_bfloat16 *)dx;
   p.ld0 = d;
   p.aux = accumulate ? (const __nv_bfloat16 *)dx : nullptr;
   p.ld_aux = d;
   p.rows_valid = T;
-  return launch_single<RDX>(mA, mB, mC, mC, p, (t_pad / BM) * p.n_tiles, s);
+  return launch_single<RDX>(mA, mB, mC, p, (t_pad / BM) * p.n_tiles, s);
 }
 
 // fp32 partials part[g] = dL_g^T x_g for the G token ranges of toff_split (in 128-row tiles).
@@ -1017,7 +720,7 @@ int tc_router_dw(const void *dl16, int64_t t_pad, int ek, const void *x, int T, 
                  const int32_t *toff_split, int G, float *part, WsHeader *hdr, cudaStream_t s) {
   using namespace tc;
   CUtensorMap mA, mB;
-  if (!make_map(&mA, dl16, t_pad, ek, MN_BOX) || !make_map(&mB, x, T, d, MN_BOX)) return MOE_ERR_CUDA;
+  if (!make_map(&mA, dl16, t_pad, ek, BK) || !make_map(&mB, x, T, d, BK)) return MOE_ERR_CUDA;
   Params p{};
   p.tile_offsets = toff_split;
   p.hdr = hdr;
@@ -1028,7 +731,7 @@ int tc_router_dw(const void *dl16, int64_t t_pad, int ek, const void *x, int T, 
   p.outf = part;
   p.ldf = d;
   p.rows_valid = E;
-  return launch_single<RDW>(mA, mB, mA, mA, p, (int64_t)G * p.m_tiles * p.n_tiles, s);
+  return launch_single<RDW>(mA, mB, mA, p, (int64_t)G * p.m_tiles * p.n_tiles, s);
 }
 
 }  // namespace moe

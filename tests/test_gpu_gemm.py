@@ -16,9 +16,10 @@ pytestmark = pytest.mark.gpu
 
 CASES = [
     # E, d, f, counts: ragged, empty, single-row and tile-multiple experts. The row-grouped kinds
-    # split an expert's c rows into ceil(c / 256) token tiles of multiples of 32 (e.g. 700 rows ->
-    # 256 + 224 + 224, 257 -> 160 + 128, 2049 -> 9 tiles), so these counts cover one- and many-tile
-    # experts, uneven splits, and tails of 1..31 rows past a multiple of 32.
+    # split an expert's c rows into full 256-token tiles and a last tile of the rest rounded up to a
+    # multiple of 32 (700 rows -> 256 + 256 + 192, 257 -> 256 + 32, 2049 -> 8 x 256 + 32), so these
+    # counts cover one- and many-tile experts, 32-token last tiles, and tails of 1..31 rows past a
+    # multiple of 32.
     (4, 512, 512, [300, 0, 129, 1]),
     (3, 256, 256, [128, 256, 5]),
     (2, 256, 768, [1, 383]),

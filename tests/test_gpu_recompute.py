@@ -17,8 +17,8 @@ from helpers import rel_err, tol_for
 pytestmark = pytest.mark.gpu
 
 CASES = [
-    moe_inputs.small("sac_pair", T=2048, d=256, E=8, k=2, f=256),          # row-grouped kinds on the CTA-pair kernel
-    moe_inputs.small("sac_single", T=300, d=256, E=8, k=2, f=512),         # single-CTA kernel
+    moe_inputs.small("sac_many_tiles", T=2048, d=256, E=8, k=2, f=256),    # several token tiles per expert
+    moe_inputs.small("sac_one_tile", T=300, d=256, E=8, k=2, f=512),       # one short token tile per expert
     moe_inputs.small("sac_f32", T=333, d=96, E=5, k=3, f=40, dtype="f32"),  # SIMT fp32 path
 ]
 

@@ -19,8 +19,8 @@ CASES = [
     ("fused_grids_exceed_gpu", [moe_inputs.small("streams_a", T=32768, d=256, E=64, k=8, f=256, seed=11),
                                 moe_inputs.small("streams_b", T=32768, d=256, E=64, k=8, f=256, routing="zipf",
                                                  alpha=1.0, seed=12)]),
-    ("pair_and_single_gemm", [moe_inputs.small("streams_c", T=3000, d=256, E=16, k=4, f=512, seed=13),
-                              moe_inputs.small("streams_d", T=2000, d=512, E=32, k=8, f=256, routing="zipf",
+    ("two_gemm_grids", [moe_inputs.small("streams_c", T=3000, d=256, E=16, k=4, f=512, seed=13),
+                        moe_inputs.small("streams_d", T=2000, d=512, E=32, k=8, f=256, routing="zipf",
                                                alpha=1.0, seed=14)]),
 ]
 KEYS = ("dx", "d_logits", "d_topk_w", "dw_gate_up", "dw_down")
