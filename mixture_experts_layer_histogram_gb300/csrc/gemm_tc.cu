@@ -401,6 +401,12 @@ __global__ void __launch_bounds__(THREADS, 1)
 // complete on the leader's full barrier; the MMA commits multicast to both CTAs' empty /
 // accumulator-full barriers; both epilogues arrive on the leader's accumulator-empty barrier. The
 // pairs run along the weight rows, so no tile is discarded; K is the expert's padded row count.
+// Tile order. A tile's time grows with its expert's rows, which vary up to about 8x the mean under
+// skewed routing. The tiles are therefore taken in order of decreasing K (experts sorted by row
+// count, ties to the lower expert id; an expert's tiles stay adjacent, so the clusters that share
+// its activations run together) and dealt to the clusters in a snake: round r gives position p to
+// cluster p on even rounds and to cluster C - 1 - p on odd ones, a static form of
+// longest-first scheduling.
 // Each ring stage costs the MMA thread one full-barrier wait and one commit, and the producer one
 // empty-barrier wait; with 64-deep stages those hand-offs held the tensor pipe to 72-77% of its
 // rate whether or not any operand was loaded, so the ring has three 128-deep stages of 64 KB.
@@ -412,7 +418,8 @@ struct PairCfg {
   static constexpr int STAGES = 3;
   static constexpr int EPI_BYTES = EPI_STAGE_BYTES;
   static constexpr int NBARS = 2 * STAGES + 5;
-  static constexpr int SMEM = STAGES * STAGE_BYTES + EPI_BYTES + 1024 + 8 * NBARS + 16;
+  static constexpr int SMEM = STAGES * STAGE_BYTES + EPI_BYTES + 1024 + 8 * NBARS + 16 + MOE_MAX_EXPERTS * 4;
+  static_assert(EPI_BYTES >= MOE_MAX_EXPERTS * 4, "the set-up borrows the epilogue buffers");
   static_assert(SMEM <= 232448, "pair kernel shared memory exceeds 227 KB");
 };
 
@@ -422,12 +429,20 @@ __host__ __device__ constexpr uint32_t idesc_bf16_pair_mn() {
          ((uint32_t)((2 * BM) >> 4) << 24);
 }
 
-// The weight-gradient tile (expert e, row pair, N tile) as seen from CTA `rank`.
-__device__ __forceinline__ Tile decode_wgrad(int tile, const Params &p, const int *toff, int rank) {
+// Tile position of round r for cluster c of C (the snake), or -1 past the last tile.
+__device__ __forceinline__ int snake_tile(int r, int c, int C, int num_tiles) {
+  const int s = r * C + ((r & 1) ? C - 1 - c : c);
+  return s < num_tiles ? s : -1;
+}
+
+// The s-th weight-gradient tile in order of decreasing K (expert order[s / per], row pair, N tile)
+// as seen from CTA `rank`.
+__device__ __forceinline__ Tile decode_wgrad(int s, const Params &p, const int *toff, const int *order, int rank) {
   Tile t;
   const int per = (p.m_tiles / 2) * p.n_tiles;
-  t.e = tile / per;
-  const int r = tile - t.e * per;
+  const int q = s / per;
+  t.e = order[q];
+  const int r = s - q * per;
   t.m0 = (r / p.n_tiles) * (2 * BM) + rank * BM;
   t.n0 = (r % p.n_tiles) * BN;
   t.krow0 = toff[t.e] * BM;
@@ -448,6 +463,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
   // bars: full[PS], empty[PS], tfull[2], tempty[2], mma_done
   uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(bars + Cfg::NBARS);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_holder + 1);
+  int *order = reinterpret_cast<int *>(tmem_holder + 4);   // experts by decreasing row count
+  int *kbs = reinterpret_cast<int *>(epi_smem);            // row tiles of each expert (set-up only)
   const int *toff = p.tile_offsets;   // read through L1; shared memory goes to the ring
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -476,6 +493,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmA)) : "memory");
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmB)) : "memory");
   }
+  for (int e = threadIdx.x; e < p.E; e += blockDim.x) kbs[e] = toff[e + 1] - toff[e];
+  __syncthreads();
+  for (int e = threadIdx.x; e < p.E; e += blockDim.x) {   // rank of e: experts with more rows, or as many and a lower id
+    const int k = kbs[e];
+    int rk = 0;
+    for (int j = 0; j < p.E; ++j) rk += (kbs[j] > k) || (kbs[j] == k && j < e);
+    order[rk] = e;
+  }
   __syncthreads();
   if (warp == 1) {   // collective TMEM allocation by one warp of each CTA of the pair
     asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_holder)),
@@ -495,8 +520,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     // ------------------------------------------------------------------ TMA producer (both CTAs)
     int stage = 0;
     uint32_t phase = 0;
-    for (int tile = cluster_id; tile < num_tiles; tile += num_clusters) {
-      const Tile t = decode_wgrad(tile, p, toff, (int)rank);
+    for (int r = 0, tile; (tile = snake_tile(r, cluster_id, num_clusters, num_tiles)) >= 0; ++r) {
+      const Tile t = decode_wgrad(tile, p, toff, order, (int)rank);
       const int bn = t.n0 + (int)rank * (BN / 2);   // this CTA's half of B
       bool ok = true;
       for (int kb = 0; kb < t.kb; ++kb) {
@@ -519,8 +544,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     int stage = 0, acc = 0;
     uint32_t phase = 0, acc_phase = 0;
     bool issued_any = false;
-    for (int tile = cluster_id; tile < num_tiles; tile += num_clusters) {
-      const Tile t = decode_wgrad(tile, p, toff, 0);
+    for (int r = 0, tile; (tile = snake_tile(r, cluster_id, num_clusters, num_tiles)) >= 0; ++r) {
+      const Tile t = decode_wgrad(tile, p, toff, order, 0);
       if (t.kb == 0) continue;
       if (!mbar_wait_cluster(tempty_bar(acc), acc_phase ^ 1u, abort_flag, p.hdr, 12)) break;
       tc_fence_after();
@@ -560,8 +585,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     EpiStore es{smem_u32(epi_smem) + (uint32_t)(warp - 2) * 2 * EPI_BUF_BYTES, 0, lane};
     int acc = 0;
     uint32_t acc_phase = 0;
-    for (int tile = cluster_id; tile < num_tiles; tile += num_clusters) {
-      const Tile t = decode_wgrad(tile, p, toff, (int)rank);
+    for (int r = 0, tile; (tile = snake_tile(r, cluster_id, num_clusters, num_tiles)) >= 0; ++r) {
+      const Tile t = decode_wgrad(tile, p, toff, order, (int)rank);
       if (t.kb == 0) {   // an expert with no rows: its gradient is zero
         __nv_bfloat16 *dst =
             p.out0 + (int64_t)t.e * p.out_e_stride + (int64_t)(t.m0 + row_in_tile) * p.ld0 + t.n0 + c0;

@@ -21,7 +21,7 @@ CASES = [
                                                  alpha=1.0, seed=12)]),
     ("two_gemm_grids", [moe_inputs.small("streams_c", T=3000, d=256, E=16, k=4, f=512, seed=13),
                         moe_inputs.small("streams_d", T=2000, d=512, E=32, k=8, f=256, routing="zipf",
-                                               alpha=1.0, seed=14)]),
+                                         alpha=1.0, seed=14)]),
 ]
 KEYS = ("dx", "d_logits", "d_topk_w", "dw_gate_up", "dw_down")
 
