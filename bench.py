@@ -190,7 +190,7 @@ def run_ours(args):
     g = inp.get("g")
     bwd = w.backward
     layer = MoELayer(w.T, w.d, w.E, w.k, w.f, w.torch_dtype, dev, backward=bwd, recompute=args.recompute,
-                     router=args.router)
+                     router=args.router, gather=args.gather)
     wr = moe_inputs.make_router_weight(w, dev) if args.router else None
     stream = torch.cuda.current_stream(dev)
     M = w.T * w.k
@@ -214,10 +214,15 @@ def run_ours(args):
                                     layer.tile_offsets, layer.row_of_slot, layer.token_of_row, layer.ws_index)
             ev[1].record(stream)
         ev[2].record(stream)
-        L.moe_permute(x, w.k, w.E, layer.row_of_slot, layer.counts, layer.tile_offsets, layer.x_perm)
+        if not args.gather:
+            L.moe_permute(x, w.k, w.E, layer.row_of_slot, layer.counts, layer.tile_offsets, layer.x_perm)
         ev[3].record(stream)
-        L.moe_grouped_ffn_fwd(layer.x_perm, wgu, wd, layer.tile_offsets, layer.offsets, layer.ab, layer.h,
-                              layer.y_perm, layer.ws_ffn)
+        if args.gather:
+            L.moe_grouped_ffn_fwd_gather(x, layer.token_of_row, wgu, wd, layer.tile_offsets, layer.offsets, layer.ab,
+                                         layer.h, layer.y_perm, layer.ws_ffn)
+        else:
+            L.moe_grouped_ffn_fwd(layer.x_perm, wgu, wd, layer.tile_offsets, layer.offsets, layer.ab, layer.h,
+                                  layer.y_perm, layer.ws_ffn)
         ev[4].record(stream)
         L.moe_combine_fwd(layer.y_perm, layer.topk_w, layer.row_of_slot, w.T, w.k, layer.out)
         ev[5].record(stream)
@@ -228,9 +233,14 @@ def run_ours(args):
         L.moe_combine_bwd(g, layer.y_perm, layer.topk_w, layer.topk_idx, layer.row_of_slot, layer.counts,
                           layer.tile_offsets, w.E, layer.dy_perm, layer.d_topk_w, layer.d_logits)
         ev[6].record(stream)
-        (L.moe_grouped_ffn_bwd_recompute if args.recompute else L.moe_grouped_ffn_bwd)(
-            layer.dy_perm, layer.x_perm, layer.ab, layer.h, wgu, wd, layer.tile_offsets, layer.offsets, layer.dab,
-            layer.dx_perm, layer.dw_gate_up, layer.dw_down, layer.ws_ffn)
+        if args.gather:
+            (L.moe_grouped_ffn_bwd_recompute_gather if args.recompute else L.moe_grouped_ffn_bwd_gather)(
+                layer.dy_perm, x, layer.token_of_row, layer.ab, layer.h, wgu, wd, layer.tile_offsets, layer.offsets,
+                layer.dab, layer.dx_perm, layer.dw_gate_up, layer.dw_down, layer.ws_ffn)
+        else:
+            (L.moe_grouped_ffn_bwd_recompute if args.recompute else L.moe_grouped_ffn_bwd)(
+                layer.dy_perm, layer.x_perm, layer.ab, layer.h, wgu, wd, layer.tile_offsets, layer.offsets, layer.dab,
+                layer.dx_perm, layer.dw_gate_up, layer.dw_down, layer.ws_ffn)
         ev[7].record(stream)
         L.moe_combine_fwd(layer.dx_perm, None, layer.row_of_slot, w.T, w.k, layer.dx)
         ev[8].record(stream)
@@ -338,7 +348,8 @@ def run_ours(args):
         "router_bwd": (3 * w.T * w.d + 2 * w.E * w.d) * es + w.T * w.E * 4,
     }
     kern = {n: {"ms": round(v, 4)} for n, v in per.items()
-            if (bwd or n in names[:5]) and (args.router or n not in ("router_bwd", "count_index"))}
+            if (bwd or n in names[:5]) and (args.router or n not in ("router_bwd", "count_index"))
+            and not (args.gather and n == "permute")}
     for n, b in mem_bytes.items():
         if n not in kern:
             continue
@@ -375,7 +386,8 @@ def run_ours(args):
         "vs_baseline": None, "dtype": w.dtype, "data": "synthetic (seeded; see moe_inputs.py)",
         "config": {"workload": w.name, "T": w.T, "d": w.d, "E": w.E, "k": w.k, "f": w.f, "routing": w.routing,
                    "pass": (("fwd+bwd (recompute)" if args.recompute else "fwd+bwd") if bwd else "fwd") +
-                           (", router GEMM in the pass" if args.router else ""),
+                           (", router GEMM in the pass" if args.router else "") +
+                           (", permutation fused into the GEMM loads" if args.gather else ""),
                    "parallelism": f"replicas x{world}", "launch": "cuda graph" if args.graph else "eager",
                    "l2": "inputs larger than L2 (expert weights 768 MiB, grouped activations > 129 MB); no flush"},
         "roofline": roofline,
@@ -467,6 +479,8 @@ def main():
                     help="the pass starts from x and router weights: router GEMM with fused top-k, and its backward")
     ap.add_argument("--graph", action="store_true",
                     help="time the steps as replays of one CUDA graph of the pass (one host launch per step)")
+    ap.add_argument("--gather", action="store_true",
+                    help="fuse the permutation into the grouped GEMMs' token loads (no moe_permute, no x_perm)")
     ap.add_argument("--recompute", action="store_true",
                     help="backward recomputes ab, h from x_perm (selective activation checkpointing)")
     ap.add_argument("--ref-tokens", type=int, default=8)

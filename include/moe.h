@@ -211,6 +211,31 @@ int moe_grouped_ffn_bwd_recompute(const void *dy_perm, const void *x_perm, void 
                                   void *dw_gate_up, void *dw_down, void *ws, size_t ws_bytes, moe_stream_t stream);
 
 /* ---------------------------------------------------------------------------------------------
+ * The grouped FFN with the permutation fused into the GEMMs' token loads (brief, section 核心方法:
+ * the generated indices feed the grouped GEMM directly). Same results, bit for bit, as
+ * moe_permute followed by the calls above, but x_perm is never formed: the tokens are passed in
+ * token order, x [T, d], with token_of_row [rows_max] from moe_count_index (-1 on padding rows,
+ * which read as zeros), and GEMM1 (forward and recompute) and the gate/up weight gradient
+ * (backward) gather their token rows through it. Every other argument, rule and result is that of
+ * the call without _gather. The bf16 kernels copy the rows with cp.async by two loader warps per
+ * CTA; entries of token_of_row outside [-1, T) read as padding rows.
+ */
+int moe_grouped_ffn_fwd_gather(const void *x, const int32_t *token_of_row, int T, const void *w_gate_up,
+                               const void *w_down, const int32_t *tile_offsets, const int32_t *offsets, int E, int d,
+                               int f, int64_t rows_max, int dtype, void *ab, void *h, void *y_perm, void *ws,
+                               size_t ws_bytes, moe_stream_t stream);
+int moe_grouped_ffn_bwd_gather(const void *dy_perm, const void *x, const int32_t *token_of_row, int T, const void *ab,
+                               const void *h, const void *w_gate_up, const void *w_down, const int32_t *tile_offsets,
+                               const int32_t *offsets, int E, int d, int f, int64_t rows_max, int dtype, void *dab,
+                               void *dx_perm, void *dw_gate_up, void *dw_down, void *ws, size_t ws_bytes,
+                               moe_stream_t stream);
+int moe_grouped_ffn_bwd_recompute_gather(const void *dy_perm, const void *x, const int32_t *token_of_row, int T,
+                                         void *ab, void *h, const void *w_gate_up, const void *w_down,
+                                         const int32_t *tile_offsets, const int32_t *offsets, int E, int d, int f,
+                                         int64_t rows_max, int dtype, void *dab, void *dx_perm, void *dw_gate_up,
+                                         void *dw_down, void *ws, size_t ws_bytes, moe_stream_t stream);
+
+/* ---------------------------------------------------------------------------------------------
  * Weighted un-permute (combine) back to token order:
  *   out[t] = sum_j topk_w[t,j] * y_perm[row_of_slot[t*k+j]]   (fp32 accumulation in slot order)
  * With topk_w == NULL the rows are summed unweighted: the backward of moe_permute

@@ -39,6 +39,11 @@ _SIGS = {
     "moe_grouped_ffn_bwd": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I64, _I, _P, _P, _P, _P, _P, _SZ, _P]),
     "moe_grouped_ffn_bwd_recompute": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I64, _I, _P, _P, _P, _P, _P,
                                            _SZ, _P]),
+    "moe_grouped_ffn_fwd_gather": (_I, [_P, _P, _I, _P, _P, _P, _P, _I, _I, _I, _I64, _I, _P, _P, _P, _P, _SZ, _P]),
+    "moe_grouped_ffn_bwd_gather": (_I, [_P, _P, _P, _I, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I64, _I, _P, _P, _P, _P, _P,
+                                        _SZ, _P]),
+    "moe_grouped_ffn_bwd_recompute_gather": (_I, [_P, _P, _P, _I, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I64, _I, _P, _P,
+                                                  _P, _P, _P, _SZ, _P]),
     "moe_combine_fwd": (_I, [_P, _P, _P, _I, _I, _I, _I64, _I, _P, _P]),
     "moe_combine_bwd": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I64, _I, _P, _P, _P, _P]),
     "moe_router_workspace_size": (_SZ, [_I, _I, _I, _I]),
@@ -178,6 +183,36 @@ def moe_grouped_ffn_bwd_recompute(dy_perm, x_perm, ab, h, w_gate_up, w_down, til
         twof // 2,
         x_perm.shape[0], dtype_code(x_perm.dtype), _p(dab), _p(dx_perm), _p(dw_gate_up), _p(dw_down), _p(ws),
         ws.numel() * ws.element_size(), _s(stream)))
+
+
+def moe_grouped_ffn_fwd_gather(x, token_of_row, w_gate_up, w_down, tile_offsets, offsets, ab, h, y_perm, ws,
+                               stream=None):
+    """moe_grouped_ffn_fwd with GEMM1 gathering its token rows from x [T, d] through token_of_row."""
+    E, twof, d = w_gate_up.shape
+    _ok("moe_grouped_ffn_fwd_gather", lib().moe_grouped_ffn_fwd_gather(
+        _p(x), _p(token_of_row), x.shape[0], _p(w_gate_up), _p(w_down), _p(tile_offsets), _p(offsets), E, d,
+        twof // 2, ab.shape[0], dtype_code(x.dtype), _p(ab), _p(h), _p(y_perm), _p(ws), ws.numel() * ws.element_size(),
+        _s(stream)))
+
+
+def moe_grouped_ffn_bwd_gather(dy_perm, x, token_of_row, ab, h, w_gate_up, w_down, tile_offsets, offsets, dab, dx_perm,
+                               dw_gate_up, dw_down, ws, stream=None):
+    """moe_grouped_ffn_bwd with the gate/up weight gradient gathering its token rows from x [T, d]."""
+    E, twof, d = w_gate_up.shape
+    _ok("moe_grouped_ffn_bwd_gather", lib().moe_grouped_ffn_bwd_gather(
+        _p(dy_perm), _p(x), _p(token_of_row), x.shape[0], _p(ab), _p(h), _p(w_gate_up), _p(w_down), _p(tile_offsets),
+        _p(offsets), E, d, twof // 2, dy_perm.shape[0], dtype_code(x.dtype), _p(dab), _p(dx_perm), _p(dw_gate_up),
+        _p(dw_down), _p(ws), ws.numel() * ws.element_size(), _s(stream)))
+
+
+def moe_grouped_ffn_bwd_recompute_gather(dy_perm, x, token_of_row, ab, h, w_gate_up, w_down, tile_offsets, offsets,
+                                         dab, dx_perm, dw_gate_up, dw_down, ws, stream=None):
+    """moe_grouped_ffn_bwd_recompute with GEMM1 and the gate/up weight gradient gathering from x [T, d]."""
+    E, twof, d = w_gate_up.shape
+    _ok("moe_grouped_ffn_bwd_recompute_gather", lib().moe_grouped_ffn_bwd_recompute_gather(
+        _p(dy_perm), _p(x), _p(token_of_row), x.shape[0], _p(ab), _p(h), _p(w_gate_up), _p(w_down), _p(tile_offsets),
+        _p(offsets), E, d, twof // 2, dy_perm.shape[0], dtype_code(x.dtype), _p(dab), _p(dx_perm), _p(dw_gate_up),
+        _p(dw_down), _p(ws), ws.numel() * ws.element_size(), _s(stream)))
 
 
 def moe_combine_fwd(y_perm, topk_w, row_of_slot, T, k, out, stream=None):

@@ -59,6 +59,9 @@ constexpr int NT_MAX = 256;           // tokens per tile: the MMA's N
 constexpr int TOK_ROWS = NT_MAX / 2;  // token rows per CTA in one B box
 constexpr int EPI_WARPS = 8;
 constexpr int THREADS = 64 + 32 * EPI_WARPS;
+constexpr int LOADER_WARPS = 2;                       // gathering GATEUP: warps per loader set, ...
+constexpr int LOADER_SETS = 3;                        // ... one set per ring slot
+constexpr int THREADS_G = THREADS + 32 * LOADER_WARPS * LOADER_SETS;
 constexpr int TMEM_COLS = 2 * NT_MAX;
 constexpr int MAX_E = MOE_MAX_EXPERTS;
 
@@ -92,6 +95,10 @@ struct Params {
   int64_t ld0;
   __nv_bfloat16 *out1;           // GATEUP h
   int64_t ld1;
+  const __nv_bfloat16 *gx;       // gathering GATEUP: the token rows x [ntok, ldgx] ...
+  const int32_t *tor;            // ... and the token of each grouped row (-1 on padding rows)
+  int64_t ldgx;
+  int ntok;
 };
 
 // Tile = (expert e, token tile i, feature tile ft). Expert e's c rows fill n = ceil(c / 256) token
@@ -144,8 +151,10 @@ __device__ __forceinline__ void zero_rows(__nv_bfloat16 *out, int64_t ld, int ro
   for (int i = 0; i < cols / 8; ++i) dst[i] = make_uint4(0, 0, 0, 0);
 }
 
-template <int K>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
+// G (GATEUP only): the token operand is gathered from x by token_of_row with cp.async by loader
+// warps, instead of being read from the permuted x_perm by TMA (the permutation fused into the load).
+template <int K, bool G>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(G ? THREADS_G : THREADS, 1)
     rows_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const __grid_constant__ CUtensorMap tmC0, const __grid_constant__ CUtensorMap tmC1, const Params p) {
   using C = Cfg<K>;
@@ -173,7 +182,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < PS; ++s) {
-      mbar_init(full_bar(s), 1);
+      // gathering: the leader's expect_tx plus one arrival per loader warp of both CTAs
+      mbar_init(full_bar(s), G ? 1 + 2 * LOADER_WARPS : 1);
       mbar_init(empty_bar(s), 1);
     }
     for (int a = 0; a < 2; ++a) {
@@ -186,7 +196,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmA)) : "memory");
-    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmB)) : "memory");
+    if (!G) asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmB)) : "memory");
   }
   if (warp == 0) {   // ttoff = exclusive scan of the token tiles per expert, ceil(rows / 256)
     int c[8], sum = 0;
@@ -238,10 +248,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
         if (!mbar_spin_cluster(empty_bar(stage), phase ^ 1u, abort_flag, p.hdr, 21)) { ok = false; break; }
         const uint32_t sA = sbase + stage * C::STAGE_BYTES, sB = sA + C::A_BYTES;
         const uint32_t fb = mapa_shared(full_bar(stage), 0);   // the leader's full barrier
-        if (leader) mbar_expect_tx(full_bar(stage), 2 * C::STAGE_BYTES);
+        if (leader) mbar_expect_tx(full_bar(stage), 2 * (G ? C::A_BYTES : C::STAGE_BYTES));
         const int kx = kb * C::BKP;
+        if (!G) {
 #pragma unroll
-        for (int a = 0; a < C::KA; ++a) tma_load_2d_pair(sB + a * (TOK_ROWS * 128), &tmB, kx + 64 * a, brow, fb);
+          for (int a = 0; a < C::KA; ++a) tma_load_2d_pair(sB + a * (TOK_ROWS * 128), &tmB, kx + 64 * a, brow, fb);
+        }
         if (K == GATEUP) {
 #pragma unroll
           for (int a = 0; a < C::KA; ++a)
@@ -298,6 +310,39 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
       const uint64_t t0 = global_ns();
       while (!mbar_try_wait(mma_done_bar, 0) && global_ns() - t0 < kWaitLimitNs) {}
     }
+  } else if (G && warp >= 2 + EPI_WARPS) {
+    // ------------------------------------------------------------------ token-row gather (both CTAs)
+    // Loader set q (two warps) fills ring slot q: every third fill. Each thread copies one 16-byte
+    // chunk (lane % 8) of 16 of the CTA's token rows per 64-deep atom into the 128-byte-swizzled
+    // K-major layout the TMA would have written; a padding row (token -1) is filled with zeros.
+    static_assert(!G || PS == LOADER_SETS, "one loader set per ring slot");
+    const int lw = warp - (2 + EPI_WARPS);
+    const int q = lw / LOADER_WARPS;
+    const int chunk = lane & 7;
+    const int rsub = (lw % LOADER_WARPS) * 4 + (lane >> 3);   // rows rsub, rsub + 8, ..., rsub + 120
+    int fill = 0;                             // fills of the ring so far (all slots)
+    uint32_t phase = 0;                       // parity of slot q's next fill
+    bool ok = true;
+    for (int tile = cluster_id; tile < num_tiles && ok; tile += num_clusters) {
+      const Tile t = decode(tile, p, ttoff);
+      const int brow = t.start + (int)rank * (t.nt >> 1), nrows = t.nt >> 1;
+      int tok[16];
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        const int row = 8 * j + rsub;
+        const int tk = row < nrows ? p.tor[brow + row] : -2;   // -2: the MMA reads no such row
+        tok[j] = tk >= p.ntok ? -1 : tk;                       // an index past the tokens reads as padding
+      }
+      for (int kb = 0; kb < p.num_kb; ++kb, ++fill) {
+        if (fill % PS != q) continue;
+        if (!mbar_spin_cluster(empty_bar(q), phase ^ 1u, abort_flag, p.hdr, 26)) { ok = false; break; }
+        phase ^= 1u;
+        gather_rows<C::KA>(sbase + q * C::STAGE_BYTES + C::A_BYTES, TOK_ROWS * 128, p.gx, p.ldgx, tok, rsub, chunk,
+                           kb * C::BKP);
+        gather_done(full_bar(q), lane);
+      }
+    }
+    asm volatile("cp.async.wait_group 0;" ::: "memory");
   } else if (warp >= 2) {
     // ------------------------------------------------------------------ epilogue (both CTAs)
     const int quarter = warp & 3;             // TMEM lanes 32 quarter .. 32 quarter + 31
@@ -494,24 +539,25 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
 }
 
 // A persistent grid of as many CTA pairs as can be resident at once (at most one per tile).
-template <int K>
+template <int K, bool G = false>
 static int launch(const CUtensorMap &a, const CUtensorMap &b, const CUtensorMap &c0, const CUtensorMap &c1,
                   const Params &p, int64_t max_tiles, cudaStream_t s) {
   constexpr int smem = Cfg<K>::SMEM;
-  MOE_TRY_CUDA(cudaFuncSetAttribute(rows_kernel<K>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem));
+  constexpr int threads = G ? THREADS_G : THREADS;
+  MOE_TRY_CUDA(cudaFuncSetAttribute(rows_kernel<K, G>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem));
   int resident = 0;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)(sm_count() / 2 * 2), 1, 1);
-  cfg.blockDim = dim3(THREADS, 1, 1);
+  cfg.blockDim = dim3(threads, 1, 1);
   cfg.dynamicSmemBytes = smem;
-  if (cudaOccupancyMaxActiveClusters(&resident, rows_kernel<K>, &cfg) != cudaSuccess || resident < 1) {
+  if (cudaOccupancyMaxActiveClusters(&resident, rows_kernel<K, G>, &cfg) != cudaSuccess || resident < 1) {
     (void)cudaGetLastError();
     resident = sm_count() / 2;
   }
   int64_t clusters = resident;
   if (max_tiles < clusters) clusters = max_tiles;
   if (clusters < 1) clusters = 1;
-  rows_kernel<K><<<(int)(2 * clusters), THREADS, smem, s>>>(a, b, c0, c1, p);
+  rows_kernel<K, G><<<(int)(2 * clusters), threads, smem, s>>>(a, b, c0, c1, p);
   MOE_CHECK_LAUNCH();
   return MOE_OK;
 }
@@ -543,6 +589,37 @@ int rows_gateup(const void *x_perm, const void *wgu, const int32_t *tile_offsets
   p.out1 = (__nv_bfloat16 *)h;
   p.ld1 = f;
   return launch<GATEUP>(mA, mB, mC0, mC1, p, (rows_max / 128) * p.n_ft, s);
+}
+
+// GEMM1 with the permutation fused into its token-operand load: rows of x [T, d] gathered by
+// token_of_row (grouped row -> token, -1 on padding rows) instead of read from x_perm.
+int rows_gateup_gather(const void *x, const int32_t *token_of_row, int T, const void *wgu, const int32_t *tile_offsets,
+                       const int32_t *offsets, int E, int d, int f, int64_t rows_max, void *ab, void *h, WsHeader *hdr,
+                       cudaStream_t s) {
+  using namespace tc;
+  using namespace tc::rows;
+  CUtensorMap mA, mC0, mC1;
+  if (!make_gateup_map(&mA, wgu, E, f, d) || !make_store_map16(&mC0, ab, rows_max, 2 * f) ||
+      !make_store_map16(&mC1, h, rows_max, f))
+    return MOE_ERR_CUDA;
+  rows::Params p{};
+  p.tile_offsets = tile_offsets;
+  p.offsets = offsets;
+  p.hdr = hdr;
+  p.E = E;
+  p.rows_max = rows_max;
+  p.n_ft = f / 128;
+  p.num_kb = d / Cfg<GATEUP>::BKP;
+  p.f = f;
+  p.out0 = (__nv_bfloat16 *)ab;
+  p.ld0 = 2 * (int64_t)f;
+  p.out1 = (__nv_bfloat16 *)h;
+  p.ld1 = f;
+  p.gx = (const __nv_bfloat16 *)x;
+  p.tor = token_of_row;
+  p.ldgx = d;
+  p.ntok = T;
+  return launch<GATEUP, true>(mA, mA, mC0, mC1, p, (rows_max / 128) * p.n_ft, s);
 }
 
 int rows_down(const void *h, const void *wd, const int32_t *tile_offsets, const int32_t *offsets, int E, int d, int f,

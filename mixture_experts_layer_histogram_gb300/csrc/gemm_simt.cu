@@ -29,6 +29,9 @@ struct Args {
   int64_t ld_aux;
   int f;
   int Mw;                  // WGRAD: rows of dW[e]
+  const int32_t *gA;       // GATEUP gathering: A row m is token gA[m] of A (-1: zero row)
+  const int32_t *gB;       // WGRAD gathering: B's k row r (a grouped row) is token gB[r] of B (-1: zero)
+  int ntok;                // tokens of the gathered operand (indices past it read as zero rows)
 };
 
 template <int KIND>
@@ -64,9 +67,19 @@ __global__ void __launch_bounds__(256) simt_gemm_kernel(const Args p) {
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       const int r = ty + 8 * i, kk = k0 + tx;
-      As[r][tx] = (m0 + r < M && kk < K) ? A[(int64_t)(m0 + r) * p.sAm + (int64_t)kk * p.sAk] : 0.0f;
+      if (KIND == GATEUP && p.gA) {
+        const int tk = (m0 + r < M && kk < K) ? p.gA[m0 + r] : -1;
+        As[r][tx] = (tk >= 0 && tk < p.ntok) ? A[(int64_t)tk * p.sAm + (int64_t)kk * p.sAk] : 0.0f;
+      } else {
+        As[r][tx] = (m0 + r < M && kk < K) ? A[(int64_t)(m0 + r) * p.sAm + (int64_t)kk * p.sAk] : 0.0f;
+      }
       const bool nb = n0 + r < p.N && kk < K;
-      Bs[r][tx] = nb ? B[(int64_t)(n0 + r) * p.sBn + (int64_t)kk * p.sBk] : 0.0f;
+      if (KIND == WGRAD && p.gB) {
+        const int tk = nb ? p.gB[(int64_t)p.toff[e] * p.BM + kk] : -1;
+        Bs[r][tx] = (tk >= 0 && tk < p.ntok) ? p.B[(int64_t)(n0 + r) * p.sBn + (int64_t)tk * p.sBk] : 0.0f;
+      } else {
+        Bs[r][tx] = nb ? B[(int64_t)(n0 + r) * p.sBn + (int64_t)kk * p.sBk] : 0.0f;
+      }
       if (KIND == GATEUP) Bs2[r][tx] = nb ? B[p.up_off + (int64_t)(n0 + r) * p.sBn + (int64_t)kk * p.sBk] : 0.0f;
     }
     __syncthreads();
@@ -116,10 +129,14 @@ static int launch(const Args &a, int64_t m_rows, int n, int gz, cudaStream_t s) 
 
 }  // namespace simt
 
-int simt_grouped_ffn_fwd(const float *x, const float *wgu, const float *wd, const int32_t *toff, int E, int d, int f,
-                         int64_t rows_max, float *ab, float *h, float *y, cudaStream_t s) {
+// x is x_perm [rows_max, d], or with token_of_row the tokens [T, d] in token order (gathered).
+int simt_grouped_ffn_fwd(const float *x, const int32_t *token_of_row, int T, const float *wgu, const float *wd,
+                         const int32_t *toff, int E, int d, int f, int64_t rows_max, float *ab, float *h, float *y,
+                         cudaStream_t s) {
   using namespace simt;
   Args a{};
+  a.gA = token_of_row;
+  a.ntok = T;
   a.toff = toff;
   a.E = E;
   a.BM = MOE_GROUP_ROWS;
@@ -137,14 +154,16 @@ int simt_grouped_ffn_fwd(const float *x, const float *wgu, const float *wd, cons
   a.B = wd; a.sBn = f; a.sBk = 1; a.sBe = (int64_t)d * f; a.up_off = 0;
   a.N = d; a.K = f;
   a.C = y; a.ldc = d; a.C2 = nullptr;
+  a.gA = nullptr;
   return launch<DOWN>(a, rows_max, d, 1, s);
 }
 
-int simt_grouped_ffn_bwd(const float *dy, const float *x, const float *ab, const float *h, const float *wgu,
-                         const float *wd, const int32_t *toff, int E, int d, int f, int64_t rows_max, float *dab,
-                         float *dx, float *dwgu, float *dwd, cudaStream_t s) {
+int simt_grouped_ffn_bwd(const float *dy, const float *x, const int32_t *token_of_row, int T, const float *ab,
+                         const float *h, const float *wgu, const float *wd, const int32_t *toff, int E, int d, int f,
+                         int64_t rows_max, float *dab, float *dx, float *dwgu, float *dwd, cudaStream_t s) {
   using namespace simt;
   Args a{};
+  a.ntok = T;
   a.toff = toff;
   a.E = E;
   a.BM = MOE_GROUP_ROWS;
@@ -169,9 +188,10 @@ int simt_grouped_ffn_bwd(const float *dy, const float *x, const float *ab, const
   a.N = f; a.Mw = d;
   a.C = dwd; a.ldc = f; a.sCe = (int64_t)d * f;
   if ((rc = launch<WGRAD>(a, d, f, E, s))) return rc;
-  // dWgu[e][i][c] = sum_r dab[r][i] x[r][c]
+  // dWgu[e][i][c] = sum_r dab[r][i] x[r][c] (x's rows gathered from the tokens when token_of_row is given)
   a.A = dab; a.sAm = 1; a.sAk = 2 * (int64_t)f;
   a.B = x; a.sBn = 1; a.sBk = d;
+  a.gB = token_of_row;
   a.N = d; a.Mw = 2 * f;
   a.C = dwgu; a.ldc = d; a.sCe = (int64_t)2 * f * d;
   return launch<WGRAD>(a, 2 * f, d, E, s);

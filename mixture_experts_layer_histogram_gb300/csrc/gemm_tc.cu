@@ -62,6 +62,10 @@ struct Params {
   const __nv_bfloat16 *aux;
   int64_t ld_aux;
   int64_t out_e_stride;
+  const __nv_bfloat16 *gx;   // WGRAD gathering: B rows are the tokens x [ntok, ldgx] of ...
+  const int32_t *tor;        // ... each grouped row (-1 on padding rows) instead of rows of x_perm
+  int64_t ldgx;
+  int ntok;
   float *outf;        // RDW: fp32 partials [groups, rows_valid, ldf]
   int64_t ldf;
   int rows_valid;     // RDX: rows of dx (tokens); RDW: rows of dWr (experts)
@@ -450,7 +454,12 @@ __device__ __forceinline__ Tile decode_wgrad(int s, const Params &p, const int *
   return t;
 }
 
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
+// G: B (x_perm for dW_gate_up) is gathered from x by token_of_row with cp.async by loader warps
+// instead of loaded by TMA (the permutation fused into the operand load): three sets of two warps,
+// one set per ring slot.
+constexpr int LOADER_WARPS = 2, LOADER_SETS = 3;
+template <bool G>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(G ? THREADS + 32 * LOADER_WARPS * LOADER_SETS : THREADS, 1)
     tc_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmC0, const Params p) {
   using Cfg = PairCfg;
@@ -480,7 +489,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < PS; ++s) {
-      mbar_init(full_bar(s), 1);
+      // gathering: the leader's expect_tx plus one arrival per loader warp of both CTAs
+      mbar_init(full_bar(s), G ? 1 + 2 * LOADER_WARPS : 1);
       mbar_init(empty_bar(s), 1);
     }
     for (int a = 0; a < 2; ++a) {
@@ -491,7 +501,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmA)) : "memory");
-    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmB)) : "memory");
+    if (!G) asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmB)) : "memory");
   }
   for (int e = threadIdx.x; e < p.E; e += blockDim.x) kbs[e] = toff[e + 1] - toff[e];
   __syncthreads();
@@ -528,12 +538,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
         if (!mbar_spin_cluster(empty_bar(stage), phase ^ 1u, abort_flag, p.hdr, 11)) { ok = false; break; }
         const uint32_t sA = sbase + stage * Cfg::STAGE_BYTES, sB = sA + Cfg::A_BYTES;
         const uint32_t fb = mapa_shared(full_bar(stage), 0);   // the leader's full barrier
-        if (leader) mbar_expect_tx(full_bar(stage), 2 * Cfg::STAGE_BYTES);
+        if (leader) mbar_expect_tx(full_bar(stage), 2 * (G ? Cfg::A_BYTES : Cfg::STAGE_BYTES));
         const int ky = t.krow0 + kb * P_BK;
 #pragma unroll
         for (int q = 0; q < 2; ++q) tma_load_2d_pair(sA + q * (P_BK * 128), &tmA, t.m0 + 64 * q, ky, fb);
+        if (!G) {
 #pragma unroll
-        for (int q = 0; q < 2; ++q) tma_load_2d_pair(sB + q * (P_BK * 128), &tmB, bn + 64 * q, ky, fb);
+          for (int q = 0; q < 2; ++q) tma_load_2d_pair(sB + q * (P_BK * 128), &tmB, bn + 64 * q, ky, fb);
+        }
         if (++stage == PS) { stage = 0; phase ^= 1u; }
       }
       if (!ok) break;
@@ -576,6 +588,37 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
       const uint64_t t0 = global_ns();
       while (!mbar_try_wait(mma_done_bar, 0) && global_ns() - t0 < kWaitLimitNs) {}
     }
+  } else if (G && warp >= 2 + EPI_WARPS) {
+    // ------------------------------------------------------------------ token-row gather (both CTAs)
+    // B's k rows are the expert's grouped rows: loader set q (two warps) fills ring slot q, every
+    // third fill, with the x rows of the stage's 128 k rows, 128 columns from this CTA's half of the
+    // N tile, two boxes of 64 (see gather_rows).
+    static_assert(PairCfg::STAGES == LOADER_SETS, "one loader set per ring slot");
+    const int lw = warp - (2 + EPI_WARPS);
+    const int q = lw / LOADER_WARPS;
+    const int chunk = lane & 7;
+    const int rsub = (lw % LOADER_WARPS) * 4 + (lane >> 3);
+    int fill = 0;
+    uint32_t phase = 0;
+    bool ok = true;
+    for (int r = 0, tile; ok && (tile = snake_tile(r, cluster_id, num_clusters, num_tiles)) >= 0; ++r) {
+      const Tile t = decode_wgrad(tile, p, toff, order, (int)rank);
+      const int bn = t.n0 + (int)rank * (BN / 2);
+      for (int kb = 0; kb < t.kb; ++kb, ++fill) {
+        if (fill % PS != q) continue;
+        int tok[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          const int tk = p.tor[t.krow0 + kb * P_BK + 8 * j + rsub];
+          tok[j] = tk >= p.ntok ? -1 : tk;   // an index past the tokens reads as padding
+        }
+        if (!mbar_spin_cluster(empty_bar(q), phase ^ 1u, abort_flag, p.hdr, 15)) { ok = false; break; }
+        phase ^= 1u;
+        gather_rows<2>(sbase + q * Cfg::STAGE_BYTES + Cfg::A_BYTES, P_BK * 128, p.gx, p.ldgx, tok, rsub, chunk, bn);
+        gather_done(full_bar(q), lane);
+      }
+    }
+    asm volatile("cp.async.wait_group 0;" ::: "memory");
   } else if (warp >= 2) {
     // ------------------------------------------------------------------ epilogue (both CTAs)
     const int quarter = warp & 3;
@@ -633,23 +676,25 @@ static int launch_single(const CUtensorMap &a, const CUtensorMap &b, const CUten
 }
 
 // The weight-gradient kind on a persistent grid of as many CTA pairs as can be resident at once.
+template <bool G>
 static int launch_wgrad(const CUtensorMap &a, const CUtensorMap &b, const CUtensorMap &c0, const Params &p,
                         int64_t max_pair_tiles, cudaStream_t s) {
   constexpr int smem = PairCfg::SMEM;
-  MOE_TRY_CUDA(cudaFuncSetAttribute(tc_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem));
+  constexpr int threads = G ? THREADS + 32 * LOADER_WARPS * LOADER_SETS : THREADS;
+  MOE_TRY_CUDA(cudaFuncSetAttribute(tc_pair_kernel<G>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem));
   int resident = 0;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)(sm_count() / 2 * 2), 1, 1);
-  cfg.blockDim = dim3(THREADS, 1, 1);
+  cfg.blockDim = dim3(threads, 1, 1);
   cfg.dynamicSmemBytes = smem;
-  if (cudaOccupancyMaxActiveClusters(&resident, tc_pair_kernel, &cfg) != cudaSuccess || resident < 1) {
+  if (cudaOccupancyMaxActiveClusters(&resident, tc_pair_kernel<G>, &cfg) != cudaSuccess || resident < 1) {
     (void)cudaGetLastError();
     resident = sm_count() / 2;
   }
   int64_t clusters = resident;
   if (max_pair_tiles < clusters) clusters = max_pair_tiles;
   if (clusters < 1) clusters = 1;
-  tc_pair_kernel<<<(int)(2 * clusters), THREADS, smem, s>>>(a, b, c0, p);
+  tc_pair_kernel<G><<<(int)(2 * clusters), threads, smem, s>>>(a, b, c0, p);
   MOE_CHECK_LAUNCH();
   return MOE_OK;
 }
@@ -659,6 +704,9 @@ static int launch_wgrad(const CUtensorMap &a, const CUtensorMap &b, const CUtens
 // Row-grouped kinds (gemm_rows.cu): weights as A, tokens as B, on CTA pairs.
 int rows_gateup(const void *x_perm, const void *wgu, const int32_t *tile_offsets, const int32_t *offsets, int E, int d,
                 int f, int64_t rows_max, void *ab, void *h, WsHeader *hdr, cudaStream_t s);
+int rows_gateup_gather(const void *x, const int32_t *token_of_row, int T, const void *wgu, const int32_t *tile_offsets,
+                       const int32_t *offsets, int E, int d, int f, int64_t rows_max, void *ab, void *h, WsHeader *hdr,
+                       cudaStream_t s);
 int rows_down(const void *h, const void *wd, const int32_t *tile_offsets, const int32_t *offsets, int E, int d, int f,
               int64_t rows_max, void *y, WsHeader *hdr, cudaStream_t s);
 int rows_dh(const void *dy, const void *wd, const void *ab, const int32_t *tile_offsets, const int32_t *offsets, int E,
@@ -666,20 +714,25 @@ int rows_dh(const void *dy, const void *wd, const void *ab, const int32_t *tile_
 int rows_dgrad(const void *dab, const void *wgu, const int32_t *tile_offsets, const int32_t *offsets, int E, int d,
                int f, int64_t rows_max, void *dx, WsHeader *hdr, cudaStream_t s);
 
-// Entry points used by the C ABI (api.cu).
-int tc_grouped_ffn_fwd(const void *x_perm, const void *wgu, const void *wd, const int32_t *tile_offsets,
-                       const int32_t *offsets, int E, int d, int f, int64_t rows_max, void *ab, void *h, void *y,
-                       WsHeader *hdr, cudaStream_t s) {
+// Entry points used by the C ABI (api.cu). The tokens come either permuted (x = x_perm [rows_max, d],
+// token_of_row = nullptr) or in token order (x [T, d] and token_of_row): then GEMM1 and the gate/up
+// weight gradient gather their token rows themselves and x_perm is never formed.
+int tc_grouped_ffn_fwd(const void *x, const int32_t *token_of_row, int T, const void *wgu, const void *wd,
+                       const int32_t *tile_offsets, const int32_t *offsets, int E, int d, int f, int64_t rows_max,
+                       void *ab, void *h, void *y, WsHeader *hdr, cudaStream_t s) {
   // GEMM1: [a | b] = x_perm Wgu^T, SwiGLU epilogue
-  int rc = rows_gateup(x_perm, wgu, tile_offsets, offsets, E, d, f, rows_max, ab, h, hdr, s);
+  int rc = token_of_row
+               ? rows_gateup_gather(x, token_of_row, T, wgu, tile_offsets, offsets, E, d, f, rows_max, ab, h, hdr, s)
+               : rows_gateup(x, wgu, tile_offsets, offsets, E, d, f, rows_max, ab, h, hdr, s);
   if (rc || y == nullptr) return rc;   // y == nullptr: GEMM1 only (recompute of ab, h)
   // GEMM2: y = h Wd^T
   return rows_down(h, wd, tile_offsets, offsets, E, d, f, rows_max, y, hdr, s);
 }
 
-int tc_grouped_ffn_bwd(const void *dy, const void *x_perm, const void *ab, const void *h, const void *wgu,
-                       const void *wd, const int32_t *tile_offsets, const int32_t *offsets, int E, int d, int f,
-                       int64_t rows_max, void *dab, void *dx, void *dwgu, void *dwd, WsHeader *hdr, cudaStream_t s) {
+int tc_grouped_ffn_bwd(const void *dy, const void *x, const int32_t *token_of_row, int T, const void *ab, const void *h,
+                       const void *wgu, const void *wd, const int32_t *tile_offsets, const int32_t *offsets, int E, int d,
+                       int f, int64_t rows_max, void *dab, void *dx, void *dwgu, void *dwd, WsHeader *hdr,
+                       cudaStream_t s) {
   using namespace tc;
   CUtensorMap mA, mB, mC;
   Params p{};
@@ -700,20 +753,28 @@ int tc_grouped_ffn_bwd(const void *dy, const void *x_perm, const void *ab, const
   p.out0 = (__nv_bfloat16 *)dwd;
   p.ld0 = f;
   p.out_e_stride = (int64_t)d * f;
-  if ((rc = launch_wgrad(mA, mB, mC, p, (int64_t)E * (p.m_tiles / 2) * p.n_tiles, s)))
+  if ((rc = launch_wgrad<false>(mA, mB, mC, p, (int64_t)E * (p.m_tiles / 2) * p.n_tiles, s)))
     return rc;
   // dx_perm = dab Wgu[e] (Wgu read MN-major)
   if ((rc = rows_dgrad(dab, wgu, tile_offsets, offsets, E, d, f, rows_max, dx, hdr, s))) return rc;
-  // dWgu[e] = dab_e^T x_perm_e
-  if (!make_map(&mA, dab, rows_max, 2 * f, PairCfg::BKP) || !make_map(&mB, x_perm, rows_max, d, PairCfg::BKP) ||
-      !make_store_map(&mC, dwgu, (uint64_t)E * 2 * f, d))
+  // dWgu[e] = dab_e^T x_perm_e (x_perm's rows gathered from x when token_of_row is given)
+  if (!make_map(&mA, dab, rows_max, 2 * f, PairCfg::BKP) || !make_store_map(&mC, dwgu, (uint64_t)E * 2 * f, d))
     return MOE_ERR_CUDA;
+  if (!token_of_row && !make_map(&mB, x, rows_max, d, PairCfg::BKP)) return MOE_ERR_CUDA;
   p.m_tiles = 2 * f / BM;
   p.n_tiles = d / BN;
   p.out0 = (__nv_bfloat16 *)dwgu;
   p.ld0 = d;
   p.out_e_stride = (int64_t)2 * f * d;
-  return launch_wgrad(mA, mB, mC, p, (int64_t)E * (p.m_tiles / 2) * p.n_tiles, s);
+  const int64_t pair_tiles = (int64_t)E * (p.m_tiles / 2) * p.n_tiles;
+  if (token_of_row) {
+    p.gx = (const __nv_bfloat16 *)x;
+    p.tor = token_of_row;
+    p.ldgx = d;
+    p.ntok = T;
+    return launch_wgrad<true>(mA, mA, mC, p, pair_tiles, s);
+  }
+  return launch_wgrad<false>(mA, mB, mC, p, pair_tiles, s);
 }
 
 // Router backward GEMMs (router.cu prepares dl16, the bf16 copy of d_logits [t_pad, ek] with zero

@@ -229,5 +229,43 @@ __device__ __forceinline__ void ldmatrix_t4(uint32_t addr, uint32_t (&m)[4]) {
                : "memory");
 }
 
+// ---------------------------------------------------------------------------------------------
+// Token-row gather into a 128-byte-swizzled ring stage (the permutation fused into a GEMM's operand
+// load). A CTA's 128 operand rows are grouped rows whose token is tok (-1: padding, filled with
+// zeros; -2: not read by the MMA, skipped); each of a loader thread's 16 rows (8 j + rsub) is copied
+// 16 bytes (chunk `chunk` of 8) per box of 64 columns. Box b covers columns col0 + 64 b and lands at
+// dst + b * box_bytes, row r at r * 128 with its chunks XOR-swizzled by r % 8, the layout a 2D TMA
+// box of 64 columns with 128-byte swizzle writes (K-major rows for a K-major operand, k rows for an
+// MN-major one).
+template <int NBOX>
+__device__ __forceinline__ void gather_rows(uint32_t dst, uint32_t box_bytes, const __nv_bfloat16 *x, int64_t ld,
+                                            const int (&tok)[16], int rsub, int chunk, int col0) {
+#pragma unroll
+  for (int b = 0; b < NBOX; ++b) {
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      if (tok[j] == -2) continue;
+      const int row = 8 * j + rsub;
+      const __nv_bfloat16 *src = tok[j] >= 0 ? x + (int64_t)tok[j] * ld + col0 + 64 * b + 8 * chunk : x;
+      const uint32_t d = dst + (uint32_t)b * box_bytes + (uint32_t)(row * 128) + ((uint32_t)(chunk ^ (row & 7)) << 4);
+      asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(d), "l"(src), "r"(tok[j] >= 0 ? 16 : 0)
+                   : "memory");
+    }
+  }
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+
+// Completion of a gathered stage: the loader warps wait for their own copies, fence them into the
+// async proxy (the tensor core reads shared memory through it), and one lane per warp arrives on
+// the leader CTA's full barrier of the stage. The gathering kernels run three loader sets of warps,
+// each owning one slot of the three-stage ring, so three stages are in flight at once and each is
+// handed over as soon as its rows have landed.
+__device__ __forceinline__ void gather_done(uint32_t full_bar_stage, int lane) {
+  asm volatile("cp.async.wait_group 0;" ::: "memory");
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  __syncwarp();
+  if (lane == 0) mbar_arrive_cluster(mapa_shared(full_bar_stage, 0));
+}
+
 }  // namespace tc
 }  // namespace moe

@@ -7,6 +7,8 @@ Forward (one stream, no host synchronisation):
     moe_count_index  topk_idx -> counts, offsets, tile_offsets, row_of_slot, token_of_row)
   moe_permute      x [T,d]             -> x_perm [rows_max,d]
   moe_grouped_ffn_fwd                  -> ab [rows_max,2f], h [rows_max,f], y_perm [rows_max,d]
+   (gather=True: no moe_permute and no x_perm; moe_grouped_ffn_fwd_gather reads x [T,d] through
+    token_of_row, and the backward's moe_grouped_ffn_bwd_gather does the same)
   moe_combine_fwd  y_perm, topk_w      -> out [T,d]
 Backward:
   moe_combine_bwd  grad_out            -> dy_perm, d_topk_w [T,k], d_logits [T,E]
@@ -28,12 +30,14 @@ class MoELayer:
     """Buffers of one layer pass, allocated once and reused every step (no allocation per step)."""
 
     def __init__(self, T, d, E, k, f, dtype=torch.bfloat16, device="cuda", backward=True, recompute=False,
-                 scratch=None, router=False):
+                 scratch=None, router=False, gather=False):
         """recompute: the backward recomputes ab and h from x_perm instead of reading them (selective
         activation checkpointing); ab and h may then live in `scratch` (a dict with tensors "ab" [R, 2f]
         and "h" [R, f] shared with other layers).
         router: the layer computes its logits from x and router weights (forward(..., w_router=W_r)),
-        and its backward adds the router's share to dx and returns dw_router."""
+        and its backward adds the router's share to dx and returns dw_router.
+        gather: the permutation is fused into the grouped GEMMs' token loads (x_perm is never formed;
+        the backward reads the x passed to forward, which must stay unchanged until then)."""
         if not torch.cuda.is_available():
             raise RuntimeError("MoELayer needs a CUDA device")
         self.T, self.d, self.E, self.k, self.f = T, d, E, k, f
@@ -53,7 +57,9 @@ class MoELayer:
         self.ws_index = torch.zeros(L.moe_count_index_workspace_size(T, k, E), dtype=torch.uint8, device=self.device)
         self.ws_ffn = torch.zeros(L.moe_grouped_ffn_workspace_size(E, d, f, R, L.dtype_code(dtype), backward),
                                   dtype=torch.uint8, device=self.device)
-        self.x_perm = torch.empty((R, d), **act)
+        self.gather = gather
+        self.x_perm = None if gather else torch.empty((R, d), **act)
+        self._xin = None
         self.recompute = recompute
         if scratch is not None:
             self.ab, self.h = scratch["ab"], scratch["h"]
@@ -95,9 +101,14 @@ class MoELayer:
             L.moe_route_count_index(logits, self.k, self.topk_idx, self.topk_w, self.counts, self.offsets,
                                     self.tile_offsets, self.row_of_slot, self.token_of_row, self.ws_index, stream)
             self._x = self._w_router = None
-        L.moe_permute(x, self.k, self.E, self.row_of_slot, self.counts, self.tile_offsets, self.x_perm, stream)
-        L.moe_grouped_ffn_fwd(self.x_perm, w_gate_up, w_down, self.tile_offsets, self.offsets, self.ab, self.h,
-                              self.y_perm, self.ws_ffn, stream)
+        if self.gather:
+            self._xin = x
+            L.moe_grouped_ffn_fwd_gather(x, self.token_of_row, w_gate_up, w_down, self.tile_offsets, self.offsets,
+                                         self.ab, self.h, self.y_perm, self.ws_ffn, stream)
+        else:
+            L.moe_permute(x, self.k, self.E, self.row_of_slot, self.counts, self.tile_offsets, self.x_perm, stream)
+            L.moe_grouped_ffn_fwd(self.x_perm, w_gate_up, w_down, self.tile_offsets, self.offsets, self.ab, self.h,
+                                  self.y_perm, self.ws_ffn, stream)
         L.moe_combine_fwd(self.y_perm, self.topk_w, self.row_of_slot, self.T, self.k, self.out, stream)
         return self.out
 
@@ -106,9 +117,14 @@ class MoELayer:
             raise RuntimeError("layer was built without backward buffers")
         L.moe_combine_bwd(grad_out, self.y_perm, self.topk_w, self.topk_idx, self.row_of_slot, self.counts,
                           self.tile_offsets, self.E, self.dy_perm, self.d_topk_w, self.d_logits, stream)
-        bwd = L.moe_grouped_ffn_bwd_recompute if self.recompute else L.moe_grouped_ffn_bwd
-        bwd(self.dy_perm, self.x_perm, self.ab, self.h, w_gate_up, w_down, self.tile_offsets, self.offsets, self.dab,
-            self.dx_perm, self.dw_gate_up, self.dw_down, self.ws_ffn, stream)
+        if self.gather:
+            bwd = L.moe_grouped_ffn_bwd_recompute_gather if self.recompute else L.moe_grouped_ffn_bwd_gather
+            bwd(self.dy_perm, self._xin, self.token_of_row, self.ab, self.h, w_gate_up, w_down, self.tile_offsets,
+                self.offsets, self.dab, self.dx_perm, self.dw_gate_up, self.dw_down, self.ws_ffn, stream)
+        else:
+            bwd = L.moe_grouped_ffn_bwd_recompute if self.recompute else L.moe_grouped_ffn_bwd
+            bwd(self.dy_perm, self.x_perm, self.ab, self.h, w_gate_up, w_down, self.tile_offsets, self.offsets,
+                self.dab, self.dx_perm, self.dw_gate_up, self.dw_down, self.ws_ffn, stream)
         L.moe_combine_fwd(self.dx_perm, None, self.row_of_slot, self.T, self.k, self.dx, stream)
         res = dict(dx=self.dx, d_logits=self.d_logits, d_topk_w=self.d_topk_w, dw_gate_up=self.dw_gate_up,
                    dw_down=self.dw_down)
@@ -150,7 +166,7 @@ class MoELayer:
         else:                                 # one fused kernel while its blocks fit at once (2 per SM)
             sms = torch.cuda.get_device_properties(self.device).multi_processor_count
             index = 1 if -(-self.T * self.k // 1024) <= 2 * sms else 3
-        fwd = index + 1 + 2 + 1
+        fwd = index + (0 if self.gather else 1) + 2 + 1
         bwd = 1 + 4 + 1 + (1 if self.recompute else 0)
         if self._w_router is not None:
             bwd += 4   # prep, dx GEMM, dW GEMM, reduce
