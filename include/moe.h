@@ -63,8 +63,19 @@ enum moe_status {
   MOE_ERR_UNSUPPORTED = -2,     /* shape or dtype outside what a kernel supports (see each call) */
   MOE_ERR_CUDA = -3,            /* a CUDA runtime call or launch failed */
   MOE_ERR_DEVICE_TIMEOUT = -4,  /* a bounded device-side wait ran out (device status word) */
-  MOE_ERR_BAD_INDEX = -5        /* an expert id outside [0, E) was seen (device status word) */
+  MOE_ERR_BAD_INDEX = -5,       /* an expert id outside [0, E) was seen (device status word) */
+  MOE_ERR_CHECK_FAILED = -6     /* a consistency check of the debug build failed (device status word):
+                                   see "Debug build" below */
 };
+
+/* Debug build. Compiled with -DMOE_CHECKS=1 (mixture_experts_layer_histogram_gb300/build.py:
+ * build(checks=True) writes libmoe_checks.so), the grouped-GEMM kernels check on the device that
+ * every tile's rows lie inside its expert's row group (offsets and tile_offsets agree: an expert's
+ * routed rows fit its padded group) and inside rows_max, that every row a tile stores, zero-fills or
+ * reads as a weight-gradient operand lies below rows_max, and that tile_offsets is non-decreasing.
+ * A failed check records MOE_ERR_CHECK_FAILED in the workspace status word and the tile is skipped:
+ * nothing is written outside the buffers and no kernel traps. The release build compiles the
+ * checks out. */
 
 /* ---------------------------------------------------------------------------------------------
  * Routing (brief, section 核心方法: expert selection feeding the token counting step).

@@ -12,14 +12,15 @@ import threading
 
 import torch
 
-LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libmoe.so")
+# MOE_LIBRARY selects another build of the same library (the debug build, libmoe_checks.so)
+LIB_PATH = os.environ.get("MOE_LIBRARY") or os.path.join(os.path.dirname(os.path.abspath(__file__)), "libmoe.so")
 
 MOE_F32, MOE_BF16 = 0, 1
 GROUP_ROWS = 128
 MAX_EXPERTS = 256
 MAX_TOPK = 16
 STATUS = {0: "MOE_OK", -1: "MOE_ERR_INVALID_ARG", -2: "MOE_ERR_UNSUPPORTED", -3: "MOE_ERR_CUDA",
-          -4: "MOE_ERR_DEVICE_TIMEOUT", -5: "MOE_ERR_BAD_INDEX"}
+          -4: "MOE_ERR_DEVICE_TIMEOUT", -5: "MOE_ERR_BAD_INDEX", -6: "MOE_ERR_CHECK_FAILED"}
 
 _lock = threading.Lock()
 _lib = None

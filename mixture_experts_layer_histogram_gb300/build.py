@@ -16,6 +16,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libmoe.so")
+LIB_CHECKS = os.path.join(PKG, "libmoe_checks.so")
 SOURCES = ["route_index.cu", "permute_combine.cu", "gemm_simt.cu", "gemm_tc.cu", "gemm_rows.cu", "router.cu", "api.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
@@ -37,17 +38,22 @@ def _deps():
     return max(os.path.getmtime(h) for h in hdrs)
 
 
-def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
+def build(force: bool = False, verbose: bool = False, extra_flags=(), checks: bool = False) -> str:
+    """checks=True: the debug build with the device-side consistency checks (-DMOE_CHECKS=1), written to
+    libmoe_checks.so next to the release library."""
     nvcc = _nvcc()
-    os.makedirs(BUILD, exist_ok=True)
+    out_dir = os.path.join(BUILD, "checks") if checks else BUILD
+    lib_path = LIB_CHECKS if checks else LIB
+    os.makedirs(out_dir, exist_ok=True)
     dep_t = _deps()
     flags = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", f"-I{INCLUDE}", f"-I{CSRC}",
-                    "--expt-relaxed-constexpr"] + list(extra_flags) + os.environ.get("MOE_NVCC_FLAGS", "").split()
+                    "--expt-relaxed-constexpr"] + (["-DMOE_CHECKS=1"] if checks else []) + list(extra_flags) + \
+        os.environ.get("MOE_NVCC_FLAGS", "").split()
     jobs = []
     objs = []
     for src in SOURCES:
         s = os.path.join(CSRC, src)
-        o = os.path.join(BUILD, src.replace(".cu", ".o"))
+        o = os.path.join(out_dir, src.replace(".cu", ".o"))
         objs.append(o)
         if force or not os.path.exists(o) or os.path.getmtime(o) < max(os.path.getmtime(s), dep_t):
             jobs.append([nvcc] + flags + ["-c", s, "-o", o])
@@ -63,13 +69,13 @@ def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
             if verbose and out.strip():
                 print(out)
     newest = max(os.path.getmtime(o) for o in objs)
-    if force or jobs or not os.path.exists(LIB) or os.path.getmtime(LIB) < newest:
+    if force or jobs or not os.path.exists(lib_path) or os.path.getmtime(lib_path) < newest:
         libdir = _cuda_lib_dir(nvcc)
-        tmp = LIB + f".tmp{os.getpid()}"
+        tmp = lib_path + f".tmp{os.getpid()}"
         run([nvcc] + ARCH + ["-shared", "-cudart", "shared", "-o", tmp] + objs +
             ["-Xlinker", f"-rpath={libdir}", f"-L{libdir}"])
-        os.replace(tmp, LIB)
-    return LIB
+        os.replace(tmp, lib_path)
+    return lib_path
 
 
 if __name__ == "__main__":

@@ -183,6 +183,7 @@ extern "C" const char *moe_status_string(int status) {
     case MOE_ERR_CUDA: return "CUDA runtime error";
     case MOE_ERR_DEVICE_TIMEOUT: return "device-side wait timed out";
     case MOE_ERR_BAD_INDEX: return "expert index out of range";
+    case MOE_ERR_CHECK_FAILED: return "consistency check failed (debug build)";
     default: return "unknown status";
   }
 }

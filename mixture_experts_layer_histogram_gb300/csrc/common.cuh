@@ -18,6 +18,12 @@
 
 #define MOE_CHECK_LAUNCH() MOE_TRY_CUDA(cudaGetLastError())
 
+// The debug build (-DMOE_CHECKS=1) compiles device-side consistency checks into the GEMM kernels;
+// a failed check records MOE_ERR_CHECK_FAILED and skips the work instead of trapping.
+#ifndef MOE_CHECKS
+#define MOE_CHECKS 0
+#endif
+
 namespace moe {
 
 // Every workspace starts with this header (the device status word first).

@@ -108,6 +108,7 @@ struct Tile {
   int start;      // first grouped row of the tile
   int nt;         // tokens (the MMA's N): a multiple of 32, at most 256
   int zero_end;   // rows [start + nt, zero_end) get zeros (the expert's padding; last tile only)
+  bool ok;        // debug build: the tile passed its consistency checks (always true otherwise)
 };
 
 __device__ __forceinline__ Tile decode(int tile, const Params &p, const int *ttoff) {
@@ -128,6 +129,13 @@ __device__ __forceinline__ Tile decode(int tile, const Params &p, const int *tto
   t.nt = last ? ((c - NT_MAX * i + 31) & ~31) : NT_MAX;
   t.start = p.tile_offsets[lo] * 128 + NT_MAX * i;
   t.zero_end = last ? p.tile_offsets[lo + 1] * 128 : t.start + t.nt;
+#if MOE_CHECKS
+  // the expert's routed rows fit its 128-row group, and the group lies inside the buffers
+  const int g0 = p.tile_offsets[lo], g1 = p.tile_offsets[lo + 1];
+  t.ok = c > 0 && g0 <= g1 && ((c + 31) & ~31) <= (g1 - g0) * 128 && (int64_t)g1 * 128 <= p.rows_max;
+#else
+  t.ok = true;
+#endif
   return t;
 }
 
@@ -241,6 +249,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(G ? THREADS_G : THRE
     uint32_t phase = 0;
     for (int tile = cluster_id; tile < num_tiles; tile += num_clusters) {
       const Tile t = decode(tile, p, ttoff);
+      if (!t.ok) {   // debug build: every role skips the tile; the producer reports it
+        report(p.hdr, MOE_ERR_CHECK_FAILED, tile);
+        continue;
+      }
       const int brow = t.start + (int)rank * (t.nt >> 1);   // this CTA's half of the tile's tokens
       const int frow = t.ft * (K == GATEUP ? 128 : 256) + (int)rank * (K == GATEUP ? 64 : 128);
       bool ok = true;
@@ -278,6 +290,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(G ? THREADS_G : THRE
     bool issued_any = false;
     for (int tile = cluster_id; tile < num_tiles; tile += num_clusters) {
       const Tile t = decode(tile, p, ttoff);
+      if (!t.ok) continue;
       if (!mbar_wait_cluster(tempty_bar(acc), acc_phase ^ 1u, abort_flag, p.hdr, 22)) break;
       tc_fence_after();
       const uint32_t d_tmem = tmem_base + (uint32_t)(acc * NT_MAX);
@@ -325,6 +338,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(G ? THREADS_G : THRE
     bool ok = true;
     for (int tile = cluster_id; tile < num_tiles && ok; tile += num_clusters) {
       const Tile t = decode(tile, p, ttoff);
+      if (!t.ok) continue;
       const int brow = t.start + (int)rank * (t.nt >> 1), nrows = t.nt >> 1;
       int tok[16];
 #pragma unroll
@@ -360,7 +374,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(G ? THREADS_G : THRE
     auto cursor_norm = [&]() {                // move the cursor to a chunk that exists
       while (ltile < num_tiles) {
         lt = decode(ltile, p, ttoff);
-        lchunks = lt.nt >> 5;
+        lchunks = lt.ok ? lt.nt >> 5 : 0;
         if (lj < lchunks) return;
         ltile += num_clusters;
         lj = hh;
@@ -388,6 +402,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(G ? THREADS_G : THRE
     uint32_t acc_phase = 0;
     for (int tile = cluster_id; tile < num_tiles; tile += num_clusters) {
       const Tile t = decode(tile, p, ttoff);
+      if (!t.ok) continue;
       if (!mbar_wait_cluster(tfull_bar(acc), acc_phase, abort_flag, p.hdr, 24)) break;
       tc_fence_after();
       const uint32_t tacc = tmem_base + lane_off + (uint32_t)(acc * NT_MAX);

@@ -69,6 +69,7 @@ struct Params {
   float *outf;        // RDW: fp32 partials [groups, rows_valid, ldf]
   int64_t ldf;
   int rows_valid;     // RDX: rows of dx (tokens); RDW: rows of dWr (experts)
+  int64_t rows_max;   // WGRAD: rows of the grouped operands (debug-build bound on the rows read)
 };
 
 // Instruction descriptor, kind::f16: D fp32, A and B bf16, M = 128, N = 256, K-major unless *_mn.
@@ -84,6 +85,7 @@ struct Tile {
   int n0;      // first output column
   int kb;      // number of BK blocks
   int krow0;   // WGRAD, RDW: first grouped row of the group
+  bool ok;     // debug build (WGRAD): the tile passed its consistency checks (always true otherwise)
 };
 
 template <int KIND>
@@ -451,6 +453,13 @@ __device__ __forceinline__ Tile decode_wgrad(int s, const Params &p, const int *
   t.n0 = (r % p.n_tiles) * BN;
   t.krow0 = toff[t.e] * BM;
   t.kb = (toff[t.e + 1] - toff[t.e]) * (BM / PairCfg::BKP);
+#if MOE_CHECKS
+  // the expert's group is non-empty-or-empty in order, and the rows it reduces over lie inside the buffers
+  t.ok = toff[t.e] <= toff[t.e + 1] && (int64_t)toff[t.e + 1] * BM <= p.rows_max;
+  if (!t.ok) t.kb = 0;
+#else
+  t.ok = true;
+#endif
   return t;
 }
 
@@ -558,7 +567,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(G ? THREADS + 32 * L
     bool issued_any = false;
     for (int r = 0, tile; (tile = snake_tile(r, cluster_id, num_clusters, num_tiles)) >= 0; ++r) {
       const Tile t = decode_wgrad(tile, p, toff, order, 0);
-      if (t.kb == 0) continue;
+      if (!t.ok || t.kb == 0) continue;
       if (!mbar_wait_cluster(tempty_bar(acc), acc_phase ^ 1u, abort_flag, p.hdr, 12)) break;
       tc_fence_after();
       const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
@@ -603,6 +612,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(G ? THREADS + 32 * L
     bool ok = true;
     for (int r = 0, tile; ok && (tile = snake_tile(r, cluster_id, num_clusters, num_tiles)) >= 0; ++r) {
       const Tile t = decode_wgrad(tile, p, toff, order, (int)rank);
+      if (!t.ok) continue;
       const int bn = t.n0 + (int)rank * (BN / 2);
       for (int kb = 0; kb < t.kb; ++kb, ++fill) {
         if (fill % PS != q) continue;
@@ -630,6 +640,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(G ? THREADS + 32 * L
     uint32_t acc_phase = 0;
     for (int r = 0, tile; (tile = snake_tile(r, cluster_id, num_clusters, num_tiles)) >= 0; ++r) {
       const Tile t = decode_wgrad(tile, p, toff, order, (int)rank);
+      if (!t.ok) continue;
       if (t.kb == 0) {   // an expert with no rows: its gradient is zero
         __nv_bfloat16 *dst =
             p.out0 + (int64_t)t.e * p.out_e_stride + (int64_t)(t.m0 + row_in_tile) * p.ld0 + t.n0 + c0;
@@ -741,6 +752,7 @@ int tc_grouped_ffn_bwd(const void *dy, const void *x, const int32_t *token_of_ro
   p.E = E;
   p.d = d;
   p.f = f;
+  p.rows_max = rows_max;
   int rc;
   // dh = dy Wd[e] (Wd read MN-major), SwiGLU backward epilogue -> dab
   if ((rc = rows_dh(dy, wd, ab, tile_offsets, offsets, E, d, f, rows_max, dab, hdr, s))) return rc;
