@@ -9,7 +9,8 @@ resident in HBM before timing starts; the expert weights (768 MiB at the default
 grouped activations exceed the 129 MB L2, so no flush is needed between steps.
 
 Timing: the K timed steps run back to back with nothing but the pass itself between two CUDA
-events on the launching stream. Per-kernel times (and the grouped GEMM's roofline) come from a
+events on the launching stream; each step is one replay of a CUDA graph of the whole pass (the
+library's calls recorded once; --eager launches them call by call instead). Per-kernel times (and the grouped GEMM's roofline) come from a
 separate pass of eager steps afterwards, with an event pair around every C-ABI call. The roofline's
 bf16 denominator follows the clocks sampled while those kernels ran: the measured burst peak,
 unless sw_power_cap was active, then the measured sustained peak; both fractions are printed.
@@ -41,7 +42,9 @@ METRIC_FWD = "MoE layer fwd tokens/s (E=64,k=8,d=2048); grouped-GEMM % BF16 peak
 # were captured. The bench reports the figure only while the sources still have that digest: once a
 # kernel changes, its traffic is unmeasured (null) until it is captured again.
 GEMM_SOURCES = ("gemm_tc.cu", "tc_ptx.cuh", "tma_host.cuh", "common.cuh")
-GEMM_TRAFFIC = {}   # workload -> (bytes per step, source digest)
+GEMM_TRAFFIC = {    # workload -> (bytes per step, source digest)
+    "fwdbwd_t8192": (5760514048, "24aeb2e33b9d5af0"),
+}
 DEFAULT_WORKLOAD = "fwdbwd_t8192"
 
 
@@ -477,8 +480,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--router", action="store_true",
                     help="the pass starts from x and router weights: router GEMM with fused top-k, and its backward")
-    ap.add_argument("--graph", action="store_true",
-                    help="time the steps as replays of one CUDA graph of the pass (one host launch per step)")
+    ap.add_argument("--eager", dest="graph", action="store_false",
+                    help="time the steps launched call by call instead of as replays of one CUDA graph of the pass")
     ap.add_argument("--gather", action="store_true",
                     help="fuse the permutation into the grouped GEMMs' token loads (no moe_permute, no x_perm)")
     ap.add_argument("--recompute", action="store_true",

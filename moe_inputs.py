@@ -12,6 +12,7 @@ printed there, so these are the synthetic stand-ins):
   fwdbwd_t8192    T=8192  d=2048 E=64  k=8 f=1024 bf16  fwd+bwd  as above
   skew_a0/.8/1.2  T=16384 d=2048 E=64  k=8 f=1024 bf16  fwd+bwd  forced-uniform / Zipf(0.8) / Zipf(1.2)
   large_a0.8      T=16384 d=4096 E=128 k=8 f=1536 bf16  fwd+bwd  Zipf(0.8)
+  large_shape_e16 T=2048  d=4096 E=16  k=8 f=1536 bf16  fwd+bwd  Zipf(0.8)  (profiling stand-in for large_a0.8)
 
 Expert weights ~ N(0, 0.02), tokens x ~ N(0, 1), grad_out ~ N(0, 1). bf16 tensors are drawn in
 fp32 and rounded to nearest-even bf16; the rounded values are the inputs both sides see.
@@ -62,6 +63,9 @@ WORKLOADS = {
     "skew_a0.8": Workload("skew_a0.8", 16384, 2048, 64, 8, 1024, "bf16", True, "zipf", 0.8),
     "skew_a1.2": Workload("skew_a1.2", 16384, 2048, 64, 8, 1024, "bf16", True, "zipf", 1.2),
     "large_a0.8": Workload("large_a0.8", 16384, 4096, 128, 8, 1536, "bf16", True, "zipf", 0.8),
+    # large_a0.8's per-expert shapes (d, f, k, Zipf(0.8), about 1,024 rows per expert) on 16 experts:
+    # a case small enough (about 1.5 GB) for multi-pass profiler captures of the same kernels
+    "large_shape_e16": Workload("large_shape_e16", 2048, 4096, 16, 8, 1536, "bf16", True, "zipf", 0.8),
 }
 
 # Each tensor has its own stream so that drawing one never shifts another.
