@@ -65,13 +65,16 @@ constexpr int THREADS_G = THREADS + 32 * LOADER_WARPS * LOADER_SETS;
 constexpr int TMEM_COLS = 2 * NT_MAX;
 constexpr int MAX_E = MOE_MAX_EXPERTS;
 
-template <int K> struct Cfg {
-  static constexpr int BKP = K == DH ? 64 : 128;             // k depth of one ring stage
+// The ring: 64-deep stages, as many as fit beside the epilogue's staging buffers (a load's latency
+// under full load is about as long for a 32 KB stage as for a 64 KB one, so more, smaller stages
+// keep more of it covered). Gathering GATEUP (G) keeps three 128-deep stages, one per loader set.
+template <int K, bool G = false> struct Cfg {
+  static constexpr int BKP = G ? 128 : 64;                   // k depth of one ring stage
   static constexpr int KA = BKP / 64;                        // 128-byte swizzle atoms along k per stage
   static constexpr int A_BYTES = LANES * BKP * 2;
   static constexpr int B_BYTES = TOK_ROWS * BKP * 2;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-  static constexpr int STAGES = K == DH ? 5 : 3;
+  static constexpr int STAGES = G ? 3 : (K == DH ? 5 : 6);
   static constexpr int BUF_BYTES = K == GATEUP ? 1024 : 2048;   // one 32-token staging block
   static constexpr int NBUF = K == DOWN || K == DGRAD ? 2 : 4;   // per warp (DH: two chunks of a + b)
   static constexpr int EPI_BYTES = EPI_WARPS * NBUF * BUF_BYTES;
@@ -165,7 +168,7 @@ template <int K, bool G>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(G ? THREADS_G : THREADS, 1)
     rows_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const __grid_constant__ CUtensorMap tmC0, const __grid_constant__ CUtensorMap tmC1, const Params p) {
-  using C = Cfg<K>;
+  using C = Cfg<K, G>;
   constexpr bool A_MN = (K == DH || K == DGRAD);
   constexpr int PS = C::STAGES;
   extern __shared__ uint8_t smem_raw[];
@@ -243,14 +246,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(G ? THREADS_G : THRE
   const int num_tiles = ttoff[p.E] * p.n_ft;
   const int cluster_id = blockIdx.x >> 1, num_clusters = gridDim.x >> 1;
 
-  if (warp == 0 && lane == 0) {
+  if (warp == 0) {
     // ------------------------------------------------------------------ TMA producer (both CTAs)
+    // The whole warp runs the loop and waits, converged; one elected lane issues the copies.
     int stage = 0;
     uint32_t phase = 0;
     for (int tile = cluster_id; tile < num_tiles; tile += num_clusters) {
       const Tile t = decode(tile, p, ttoff);
       if (!t.ok) {   // debug build: every role skips the tile; the producer reports it
-        report(p.hdr, MOE_ERR_CHECK_FAILED, tile);
+        if (lane == 0) report(p.hdr, MOE_ERR_CHECK_FAILED, tile);
         continue;
       }
       const int brow = t.start + (int)rank * (t.nt >> 1);   // this CTA's half of the tile's tokens
@@ -258,6 +262,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(G ? THREADS_G : THRE
       bool ok = true;
       for (int kb = 0; kb < p.num_kb; ++kb) {
         if (!mbar_spin_cluster(empty_bar(stage), phase ^ 1u, abort_flag, p.hdr, 21)) { ok = false; break; }
+        if (elect_one()) {
         const uint32_t sA = sbase + stage * C::STAGE_BYTES, sB = sA + C::A_BYTES;
         const uint32_t fb = mapa_shared(full_bar(stage), 0);   // the leader's full barrier
         if (leader) mbar_expect_tx(full_bar(stage), 2 * (G ? C::A_BYTES : C::STAGE_BYTES));
@@ -279,15 +284,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(G ? THREADS_G : THRE
           for (int q = 0; q < 2; ++q)
             tma_load_2d_pair(sA + q * (C::BKP * 128), &tmA, frow + 64 * q, t.e * p.a_rows_e + kx, fb);
         }
+        }
+        __syncwarp();
         if (++stage == PS) { stage = 0; phase ^= 1u; }
       }
       if (!ok) break;
     }
-  } else if (warp == 1 && lane == 0 && leader) {
+  } else if (warp == 1 && leader) {
     // ------------------------------------------------------------------ MMA issuer (leader only)
+    // The whole warp runs the loop and waits, converged; one elected lane issues the MMAs. The
+    // operand descriptors are formed once: every shared-memory address here lies below 256 KB, so a
+    // stage's or a k step's offset adds to the descriptor's start-address field without carry.
     int stage = 0, acc = 0;
     uint32_t phase = 0, acc_phase = 0;
     bool issued_any = false;
+    const uint64_t desc_a0 = A_MN ? sdesc(sbase, C::BKP * 128, 1024) : sdesc(sbase, 16, 1024);
+    const uint64_t desc_b0 = sdesc(sbase + C::A_BYTES, 16, 1024);
     for (int tile = cluster_id; tile < num_tiles; tile += num_clusters) {
       const Tile t = decode(tile, p, ttoff);
       if (!t.ok) continue;
@@ -299,27 +311,32 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(G ? THREADS_G : THRE
       for (int kb = 0; kb < p.num_kb; ++kb) {
         if (!mbar_spin_cluster(full_bar(stage), phase, abort_flag, p.hdr, 23)) { ok = false; break; }
         tc_fence_after();
-        const uint32_t sA = sbase + stage * C::STAGE_BYTES, sB = sA + C::A_BYTES;
+        if (elect_one()) {
+          const uint32_t so = (uint32_t)(stage * C::STAGE_BYTES) >> 4;
 #pragma unroll
-        for (int kk = 0; kk < C::BKP / 16; ++kk) {
-          // K-major: atom kk/4 (128 rows x 128 B each), 32 B per 16-deep step inside the atom.
-          // MN-major A: 2048 B per 16 k-rows; its two 64-feature blocks are BKP * 128 B apart.
-          const uint32_t koff = (uint32_t)((kk >> 2) * (LANES * 128) + (kk & 3) * 32);
-          const uint64_t ad = A_MN ? sdesc(sA + kk * 2048, C::BKP * 128, 1024) : sdesc(sA + koff, 16, 1024);
-          const uint64_t bd = sdesc(sB + koff, 16, 1024);
-          mma_bf16_pair(d_tmem, ad, bd, id, (kb | kk) != 0 ? 1u : 0u);
+          for (int kk = 0; kk < C::BKP / 16; ++kk) {
+            // K-major: atom kk/4 (128 rows x 128 B each), 32 B per 16-deep step inside the atom.
+            // MN-major A: 2048 B per 16 k-rows; its two 64-feature blocks are BKP * 128 B apart.
+            const uint32_t koff = (uint32_t)((kk >> 2) * (LANES * 128) + (kk & 3) * 32) >> 4;
+            const uint64_t ad = desc_a0 + so + (A_MN ? (uint32_t)(kk * 2048 >> 4) : koff);
+            const uint64_t bd = desc_b0 + so + koff;
+            mma_bf16_pair(d_tmem, ad, bd, id, (kb | kk) != 0 ? 1u : 0u);
+          }
+          mma_commit_pair(empty_bar(stage), 0x3);   // frees this stage in both CTAs
         }
+        __syncwarp();
         issued_any = true;
-        mma_commit_pair(empty_bar(stage), 0x3);   // frees this stage in both CTAs
         if (++stage == PS) { stage = 0; phase ^= 1u; }
       }
       if (!ok) break;
-      mma_commit_pair(tfull_bar(acc), 0x3);       // both CTAs' accumulators are ready
+      if (elect_one()) mma_commit_pair(tfull_bar(acc), 0x3);   // both CTAs' accumulators are ready
+      __syncwarp();
       acc ^= 1;
       if (acc == 0) acc_phase ^= 1u;
     }
     if (issued_any) {
-      mma_commit_pair(mma_done_bar, 0x1);
+      if (elect_one()) mma_commit_pair(mma_done_bar, 0x1);
+      __syncwarp();
       const uint64_t t0 = global_ns();
       while (!mbar_try_wait(mma_done_bar, 0) && global_ns() - t0 < kWaitLimitNs) {}
     }
@@ -557,7 +574,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(G ? THREADS_G : THRE
 template <int K, bool G = false>
 static int launch(const CUtensorMap &a, const CUtensorMap &b, const CUtensorMap &c0, const CUtensorMap &c1,
                   const Params &p, int64_t max_tiles, cudaStream_t s) {
-  constexpr int smem = Cfg<K>::SMEM;
+  constexpr int smem = Cfg<K, G>::SMEM;
   constexpr int threads = G ? THREADS_G : THREADS;
   MOE_TRY_CUDA(cudaFuncSetAttribute(rows_kernel<K, G>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem));
   int resident = 0;
@@ -624,7 +641,7 @@ int rows_gateup_gather(const void *x, const int32_t *token_of_row, int T, const 
   p.E = E;
   p.rows_max = rows_max;
   p.n_ft = f / 128;
-  p.num_kb = d / Cfg<GATEUP>::BKP;
+  p.num_kb = d / Cfg<GATEUP, true>::BKP;
   p.f = f;
   p.out0 = (__nv_bfloat16 *)ab;
   p.ld0 = 2 * (int64_t)f;

@@ -413,15 +413,15 @@ __global__ void __launch_bounds__(THREADS, 1)
 // its activations run together) and dealt to the clusters in a snake: round r gives position p to
 // cluster p on even rounds and to cluster C - 1 - p on odd ones, a static form of
 // longest-first scheduling.
-// Each ring stage costs the MMA thread one full-barrier wait and one commit, and the producer one
-// empty-barrier wait; with 64-deep stages those hand-offs held the tensor pipe to 72-77% of its
-// rate whether or not any operand was loaded, so the ring has three 128-deep stages of 64 KB.
-struct PairCfg {
-  static constexpr int BKP = 128;                         // k depth of one ring stage
+// The ring has six 64-deep stages of 32 KB: a load's latency under full load is about as long for
+// 32 KB as for 64 KB, so six small stages keep more of it covered than three large ones. Gathering
+// (G) keeps three 128-deep stages, one per loader set.
+template <bool G> struct PairCfg {
+  static constexpr int BKP = G ? 128 : 64;                // k depth of one ring stage
   static constexpr int A_BYTES = BM * BKP * 2;            // this CTA's 128 rows of A
   static constexpr int B_BYTES = (BN / 2) * BKP * 2;      // this CTA's half of B
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-  static constexpr int STAGES = 3;
+  static constexpr int STAGES = G ? 3 : 6;
   static constexpr int EPI_BYTES = EPI_STAGE_BYTES;
   static constexpr int NBARS = 2 * STAGES + 5;
   static constexpr int SMEM = STAGES * STAGE_BYTES + EPI_BYTES + 1024 + 8 * NBARS + 16 + MOE_MAX_EXPERTS * 4;
@@ -442,8 +442,9 @@ __device__ __forceinline__ int snake_tile(int r, int c, int C, int num_tiles) {
 }
 
 // The s-th weight-gradient tile in order of decreasing K (expert order[s / per], row pair, N tile)
-// as seen from CTA `rank`.
-__device__ __forceinline__ Tile decode_wgrad(int s, const Params &p, const int *toff, const int *order, int rank) {
+// as seen from CTA `rank`; t.kb counts ring stages of bkp rows.
+__device__ __forceinline__ Tile decode_wgrad(int s, const Params &p, const int *toff, const int *order, int rank,
+                                             int bkp) {
   Tile t;
   const int per = (p.m_tiles / 2) * p.n_tiles;
   const int q = s / per;
@@ -452,7 +453,7 @@ __device__ __forceinline__ Tile decode_wgrad(int s, const Params &p, const int *
   t.m0 = (r / p.n_tiles) * (2 * BM) + rank * BM;
   t.n0 = (r % p.n_tiles) * BN;
   t.krow0 = toff[t.e] * BM;
-  t.kb = (toff[t.e + 1] - toff[t.e]) * (BM / PairCfg::BKP);
+  t.kb = (toff[t.e + 1] - toff[t.e]) * (BM / bkp);
 #if MOE_CHECKS
   // the expert's group is non-empty-or-empty in order, and the rows it reduces over lie inside the buffers
   t.ok = toff[t.e] <= toff[t.e + 1] && (int64_t)toff[t.e + 1] * BM <= p.rows_max;
@@ -471,7 +472,7 @@ template <bool G>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(G ? THREADS + 32 * LOADER_WARPS * LOADER_SETS : THREADS, 1)
     tc_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmC0, const Params p) {
-  using Cfg = PairCfg;
+  using Cfg = PairCfg<G>;
   constexpr int PS = Cfg::STAGES;
   constexpr int P_BK = Cfg::BKP;
   extern __shared__ uint8_t smem_raw[];
@@ -535,38 +536,47 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(G ? THREADS + 32 * L
   const int num_tiles = p.E * (p.m_tiles / 2) * p.n_tiles;
   const int cluster_id = blockIdx.x >> 1, num_clusters = gridDim.x >> 1;
 
-  if (warp == 0 && lane == 0) {
+  if (warp == 0) {
     // ------------------------------------------------------------------ TMA producer (both CTAs)
+    // The whole warp runs the loop and waits, converged; one elected lane issues the copies.
     int stage = 0;
     uint32_t phase = 0;
     for (int r = 0, tile; (tile = snake_tile(r, cluster_id, num_clusters, num_tiles)) >= 0; ++r) {
-      const Tile t = decode_wgrad(tile, p, toff, order, (int)rank);
+      const Tile t = decode_wgrad(tile, p, toff, order, (int)rank, P_BK);
       const int bn = t.n0 + (int)rank * (BN / 2);   // this CTA's half of B
       bool ok = true;
       for (int kb = 0; kb < t.kb; ++kb) {
         if (!mbar_spin_cluster(empty_bar(stage), phase ^ 1u, abort_flag, p.hdr, 11)) { ok = false; break; }
-        const uint32_t sA = sbase + stage * Cfg::STAGE_BYTES, sB = sA + Cfg::A_BYTES;
-        const uint32_t fb = mapa_shared(full_bar(stage), 0);   // the leader's full barrier
-        if (leader) mbar_expect_tx(full_bar(stage), 2 * (G ? Cfg::A_BYTES : Cfg::STAGE_BYTES));
-        const int ky = t.krow0 + kb * P_BK;
+        if (elect_one()) {
+          const uint32_t sA = sbase + stage * Cfg::STAGE_BYTES, sB = sA + Cfg::A_BYTES;
+          const uint32_t fb = mapa_shared(full_bar(stage), 0);   // the leader's full barrier
+          if (leader) mbar_expect_tx(full_bar(stage), 2 * (G ? Cfg::A_BYTES : Cfg::STAGE_BYTES));
+          const int ky = t.krow0 + kb * P_BK;
 #pragma unroll
-        for (int q = 0; q < 2; ++q) tma_load_2d_pair(sA + q * (P_BK * 128), &tmA, t.m0 + 64 * q, ky, fb);
-        if (!G) {
+          for (int q = 0; q < 2; ++q) tma_load_2d_pair(sA + q * (P_BK * 128), &tmA, t.m0 + 64 * q, ky, fb);
+          if (!G) {
 #pragma unroll
-          for (int q = 0; q < 2; ++q) tma_load_2d_pair(sB + q * (P_BK * 128), &tmB, bn + 64 * q, ky, fb);
+            for (int q = 0; q < 2; ++q) tma_load_2d_pair(sB + q * (P_BK * 128), &tmB, bn + 64 * q, ky, fb);
+          }
         }
+        __syncwarp();
         if (++stage == PS) { stage = 0; phase ^= 1u; }
       }
       if (!ok) break;
     }
-  } else if (warp == 1 && lane == 0 && leader) {
+  } else if (warp == 1 && leader) {
     // ------------------------------------------------------------------ MMA issuer (leader only)
+    // The whole warp runs the loop and waits, converged; one elected lane issues the MMAs. The
+    // operand descriptors are formed once: every shared-memory address here lies below 256 KB, so a
+    // stage's or a k step's offset adds to the descriptor's start-address field without carry.
     constexpr uint32_t idesc = idesc_bf16_pair_mn();
     int stage = 0, acc = 0;
     uint32_t phase = 0, acc_phase = 0;
     bool issued_any = false;
+    const uint64_t desc_a0 = sdesc(sbase, P_BK * 128, 1024);
+    const uint64_t desc_b0 = sdesc(sbase + Cfg::A_BYTES, P_BK * 128, 1024);
     for (int r = 0, tile; (tile = snake_tile(r, cluster_id, num_clusters, num_tiles)) >= 0; ++r) {
-      const Tile t = decode_wgrad(tile, p, toff, order, 0);
+      const Tile t = decode_wgrad(tile, p, toff, order, 0, P_BK);
       if (!t.ok || t.kb == 0) continue;
       if (!mbar_wait_cluster(tempty_bar(acc), acc_phase ^ 1u, abort_flag, p.hdr, 12)) break;
       tc_fence_after();
@@ -575,25 +585,29 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(G ? THREADS + 32 * L
       for (int kb = 0; kb < t.kb; ++kb) {
         if (!mbar_spin_cluster(full_bar(stage), phase, abort_flag, p.hdr, 13)) { ok = false; break; }
         tc_fence_after();
-        const uint32_t sA = sbase + stage * Cfg::STAGE_BYTES, sB = sA + Cfg::A_BYTES;
+        if (elect_one()) {
+          const uint32_t so = (uint32_t)(stage * Cfg::STAGE_BYTES) >> 4;
 #pragma unroll
-        for (int kk = 0; kk < P_BK / 16; ++kk) {
-          // MN-major: 2048 B per 16 k-rows; the two 64-wide MN blocks are P_BK * 128 B apart.
-          const uint64_t ad = sdesc(sA + kk * 2048, P_BK * 128, 1024);
-          const uint64_t bd = sdesc(sB + kk * 2048, P_BK * 128, 1024);
-          mma_bf16_pair(d_tmem, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
+          for (int kk = 0; kk < P_BK / 16; ++kk) {
+            // MN-major: 2048 B per 16 k-rows; the two 64-wide MN blocks are P_BK * 128 B apart.
+            const uint32_t ko = (uint32_t)(kk * 2048) >> 4;
+            mma_bf16_pair(d_tmem, desc_a0 + so + ko, desc_b0 + so + ko, idesc, (kb | kk) != 0 ? 1u : 0u);
+          }
+          mma_commit_pair(empty_bar(stage), 0x3);   // frees this stage in both CTAs
         }
+        __syncwarp();
         issued_any = true;
-        mma_commit_pair(empty_bar(stage), 0x3);   // frees this stage in both CTAs
         if (++stage == PS) { stage = 0; phase ^= 1u; }
       }
       if (!ok) break;
-      mma_commit_pair(tfull_bar(acc), 0x3);       // both CTAs' accumulators are ready
+      if (elect_one()) mma_commit_pair(tfull_bar(acc), 0x3);   // both CTAs' accumulators are ready
+      __syncwarp();
       acc ^= 1;
       if (acc == 0) acc_phase ^= 1u;
     }
     if (issued_any) {
-      mma_commit_pair(mma_done_bar, 0x1);
+      if (elect_one()) mma_commit_pair(mma_done_bar, 0x1);
+      __syncwarp();
       const uint64_t t0 = global_ns();
       while (!mbar_try_wait(mma_done_bar, 0) && global_ns() - t0 < kWaitLimitNs) {}
     }
@@ -602,7 +616,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(G ? THREADS + 32 * L
     // B's k rows are the expert's grouped rows: loader set q (two warps) fills ring slot q, every
     // third fill, with the x rows of the stage's 128 k rows, 128 columns from this CTA's half of the
     // N tile, two boxes of 64 (see gather_rows).
-    static_assert(PairCfg::STAGES == LOADER_SETS, "one loader set per ring slot");
+    static_assert(!G || (Cfg::STAGES == LOADER_SETS && P_BK == 128), "one loader set of 128 rows per ring slot");
     const int lw = warp - (2 + EPI_WARPS);
     const int q = lw / LOADER_WARPS;
     const int chunk = lane & 7;
@@ -611,7 +625,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(G ? THREADS + 32 * L
     uint32_t phase = 0;
     bool ok = true;
     for (int r = 0, tile; ok && (tile = snake_tile(r, cluster_id, num_clusters, num_tiles)) >= 0; ++r) {
-      const Tile t = decode_wgrad(tile, p, toff, order, (int)rank);
+      const Tile t = decode_wgrad(tile, p, toff, order, (int)rank, P_BK);
       if (!t.ok) continue;
       const int bn = t.n0 + (int)rank * (BN / 2);
       for (int kb = 0; kb < t.kb; ++kb, ++fill) {
@@ -639,7 +653,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(G ? THREADS + 32 * L
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int r = 0, tile; (tile = snake_tile(r, cluster_id, num_clusters, num_tiles)) >= 0; ++r) {
-      const Tile t = decode_wgrad(tile, p, toff, order, (int)rank);
+      const Tile t = decode_wgrad(tile, p, toff, order, (int)rank, P_BK);
       if (!t.ok) continue;
       if (t.kb == 0) {   // an expert with no rows: its gradient is zero
         __nv_bfloat16 *dst =
@@ -690,7 +704,7 @@ static int launch_single(const CUtensorMap &a, const CUtensorMap &b, const CUten
 template <bool G>
 static int launch_wgrad(const CUtensorMap &a, const CUtensorMap &b, const CUtensorMap &c0, const Params &p,
                         int64_t max_pair_tiles, cudaStream_t s) {
-  constexpr int smem = PairCfg::SMEM;
+  constexpr int smem = PairCfg<G>::SMEM;
   constexpr int threads = G ? THREADS + 32 * LOADER_WARPS * LOADER_SETS : THREADS;
   MOE_TRY_CUDA(cudaFuncSetAttribute(tc_pair_kernel<G>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem));
   int resident = 0;
@@ -757,7 +771,7 @@ int tc_grouped_ffn_bwd(const void *dy, const void *x, const int32_t *token_of_ro
   // dh = dy Wd[e] (Wd read MN-major), SwiGLU backward epilogue -> dab
   if ((rc = rows_dh(dy, wd, ab, tile_offsets, offsets, E, d, f, rows_max, dab, hdr, s))) return rc;
   // dWd[e] = dy_e^T h_e (the weight-gradient kind runs on the CTA-pair kernel, whose stage depth its maps take)
-  if (!make_map(&mA, dy, rows_max, d, PairCfg::BKP) || !make_map(&mB, h, rows_max, f, PairCfg::BKP) ||
+  if (!make_map(&mA, dy, rows_max, d, PairCfg<false>::BKP) || !make_map(&mB, h, rows_max, f, PairCfg<false>::BKP) ||
       !make_store_map(&mC, dwd, (uint64_t)E * d, f))
     return MOE_ERR_CUDA;
   p.m_tiles = d / BM;
@@ -770,9 +784,10 @@ int tc_grouped_ffn_bwd(const void *dy, const void *x, const int32_t *token_of_ro
   // dx_perm = dab Wgu[e] (Wgu read MN-major)
   if ((rc = rows_dgrad(dab, wgu, tile_offsets, offsets, E, d, f, rows_max, dx, hdr, s))) return rc;
   // dWgu[e] = dab_e^T x_perm_e (x_perm's rows gathered from x when token_of_row is given)
-  if (!make_map(&mA, dab, rows_max, 2 * f, PairCfg::BKP) || !make_store_map(&mC, dwgu, (uint64_t)E * 2 * f, d))
+  const int bkp = token_of_row ? PairCfg<true>::BKP : PairCfg<false>::BKP;
+  if (!make_map(&mA, dab, rows_max, 2 * f, bkp) || !make_store_map(&mC, dwgu, (uint64_t)E * 2 * f, d))
     return MOE_ERR_CUDA;
-  if (!token_of_row && !make_map(&mB, x, rows_max, d, PairCfg::BKP)) return MOE_ERR_CUDA;
+  if (!token_of_row && !make_map(&mB, x, rows_max, d, bkp)) return MOE_ERR_CUDA;
   p.m_tiles = 2 * f / BM;
   p.n_tiles = d / BN;
   p.out0 = (__nv_bfloat16 *)dwgu;

@@ -91,6 +91,17 @@ __device__ __forceinline__ uint64_t sdesc(uint32_t saddr, uint32_t lbo, uint32_t
 }
 
 
+// One lane of the converged warp (elect.sync): the warp stays converged around the single-lane work.
+__device__ __forceinline__ bool elect_one() {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "elect.sync _|p, 0xffffffff;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(r));
+  return r != 0;
+}
+
 // ---------------------------------------------------------------------------------------------
 // CTA-pair (cta_group::2) variants: a cluster of two CTAs on one TPC shares one MMA of M = 256.
 __device__ __forceinline__ uint32_t cluster_ctarank() {
@@ -137,9 +148,9 @@ static __device__ __noinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t par
   }
 }
 // The same bounded wait, polling with mbarrier.test_wait, which never suspends the thread. For the
-// two single-thread roles of the pair GEMM's ring (the TMA producer and the MMA issuer): a phase that
-// completes is seen a little sooner than through try_wait's suspend-and-wake, which shortens the
-// hand-off every ring stage costs.
+// two roles of the pair GEMMs' rings (the TMA producer and the MMA issuer, each a converged warp): a
+// phase that completes is seen a little sooner than through try_wait's suspend-and-wake, which
+// shortens the hand-off every ring stage costs.
 static __device__ __forceinline__ bool mbar_spin_cluster(uint32_t bar, uint32_t parity, volatile int *abort_flag,
                                                          WsHeader *hdr, int where) {
   const uint64_t t0 = global_ns();
