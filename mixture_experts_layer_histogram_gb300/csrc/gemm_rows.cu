@@ -78,7 +78,7 @@ template <int K, bool G = false> struct Cfg {
   static constexpr int BUF_BYTES = K == GATEUP ? 1024 : 2048;   // one 32-token staging block
   static constexpr int NBUF = K == DOWN || K == DGRAD ? 2 : 4;   // per warp (DH: two chunks of a + b)
   static constexpr int EPI_BYTES = EPI_WARPS * NBUF * BUF_BYTES;
-  static constexpr int NBARS = 2 * STAGES + 5 + (K == DH ? 2 * EPI_WARPS : 0);
+  static constexpr int NBARS = 2 * STAGES + 5;
   static constexpr int SMEM = STAGES * STAGE_BYTES + EPI_BYTES + 1024 + 8 * NBARS + 16 + (MAX_E + 1) * 4;
   static_assert(SMEM <= 232448, "row-grouped GEMM shared memory exceeds 227 KB");
   static_assert(A_BYTES == B_BYTES, "A and B atoms share one k-offset table");
@@ -100,6 +100,7 @@ struct Params {
   int64_t ld1;
   const __nv_bfloat16 *gx;       // gathering GATEUP: the token rows x [ntok, ldgx] ...
   const int32_t *tor;            // ... and the token of each grouped row (-1 on padding rows)
+  const __nv_bfloat16 *in0;      // DH: the saved a, b [rows, 2f] (row stride ld0)
   int64_t ldgx;
   int ntok;
 };
@@ -202,8 +203,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(G ? THREADS_G : THRE
       mbar_init(tempty_bar(a), 2 * EPI_WARPS);   // one arrival per epilogue warp of both CTAs
     }
     mbar_init(mma_done_bar, 1);
-    if (K == DH)
-      for (int i = 0; i < 2 * EPI_WARPS; ++i) mbar_init(bar0 + 8u * (2 * PS + 5 + i), 1);
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmA)) : "memory");
@@ -382,33 +381,46 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(G ? THREADS_G : THRE
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
     const int mi = lane >> 3, mrow = lane & 7;   // stmatrix / ldmatrix: matrix and row this lane addresses
     int bi = 0;                               // next staging buffer (GATEUP, DOWN, DGRAD)
-    // DH: the saved a, b of a chunk arrive by TMA two chunks ahead into one of two buffer pairs
-    const uint32_t lbar = bar0 + 8u * (2 * PS + 5 + 2 * (warp - 2));
-    uint32_t lphase = 0;
+    // DH: the saved a, b of a chunk arrive two chunks ahead into one of two buffer pairs, copied by
+    // the warp itself with cp.async (one commit group per chunk): TMA copies would queue behind the
+    // ring's loads in the SM's TMA unit, and the warp would stall issuing them.
     int ltile = cluster_id, lj = hh;          // DH load cursor: next (tile, chunk) of this warp to bring in
     Tile lt{};
     int lchunks = 0;
+    bool ldecoded = false;                    // lt describes ltile (decode reads global memory: once per tile)
     auto cursor_norm = [&]() {                // move the cursor to a chunk that exists
       while (ltile < num_tiles) {
-        lt = decode(ltile, p, ttoff);
-        lchunks = lt.ok ? lt.nt >> 5 : 0;
+        if (!ldecoded) {
+          lt = decode(ltile, p, ttoff);
+          lchunks = lt.ok ? lt.nt >> 5 : 0;
+          ldecoded = true;
+        }
         if (lj < lchunks) return;
         ltile += num_clusters;
         lj = hh;
+        ldecoded = false;
       }
     };
-    auto issue_load = [&](int b) {
-      if (K != DH || ltile >= num_tiles) return;
-      if (lane == 0) {
-        asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");   // the buffer's last store has read it
-        const uint32_t dst = wbuf + (uint32_t)b * (2 * C::BUF_BYTES), bar = lbar + 8u * b;
-        const int x = lt.ft * 256 + (int)rank * 128 + quarter * 32, y = lt.start + 32 * lj;
-        mbar_expect_tx(bar, 2 * C::BUF_BYTES);
-        tma_load_2d(dst, &tmC1, x, y, bar);
-        tma_load_2d(dst + C::BUF_BYTES, &tmC1, p.f + x, y, bar);
+    auto issue_load = [&](int b) {   // DH: one commit group, empty past the last chunk
+      if (K != DH) return;
+      if (ltile < num_tiles) {
+        // lane: 16-byte column q of token rows lane / 4 + 8 i, into the 64-byte-swizzled layout
+        const uint32_t dst = wbuf + (uint32_t)b * (2 * C::BUF_BYTES);
+        const int x = lt.ft * 256 + (int)rank * 128 + quarter * 32, y = lt.start + 32 * lj, q = lane & 3;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int t = (lane >> 2) + 8 * i;
+          const uint32_t so = (uint32_t)t * 64 + ((uint32_t)(q ^ ((t >> 1) & 3)) << 4);
+          if (y + t < p.rows_max) {
+            const __nv_bfloat16 *src = p.in0 + (int64_t)(y + t) * p.ld0 + x + 8 * q;
+            cp_async16(dst + so, src);
+            cp_async16(dst + C::BUF_BYTES + so, src + p.f);
+          }
+        }
+        lj += 2;
+        cursor_norm();
       }
-      lj += 2;
-      cursor_norm();
+      asm volatile("cp.async.commit_group;" ::: "memory");
     };
     if (K == DH) {
       cursor_norm();
@@ -471,8 +483,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(G ? THREADS_G : THRE
             bi = (bi + 1) & (C::NBUF - 1);
           }
         } else if (K == DH) {
-          if (!mbar_wait_cluster(lbar + 8u * bi, (lphase >> bi) & 1u, abort_flag, p.hdr, 25)) { ok = false; break; }
-          lphase ^= 1u << bi;
+          asm volatile("cp.async.wait_group 1;" ::: "memory");   // this chunk's group; the next one may be in flight
+          __syncwarp();
           const uint32_t abuf = wbuf + (uint32_t)bi * (2 * C::BUF_BYTES), bbuf = abuf + C::BUF_BYTES;
           tmem_ld_wait();
 #pragma unroll
@@ -502,14 +514,26 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(G ? THREADS_G : THRE
             stmatrix_t4(abuf + off, da[0], da[1], da[2], da[3]);
             stmatrix_t4(bbuf + off, db[0], db[1], db[2], db[3]);
           }
-          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
           __syncwarp();
-          if (lane == 0) {
-            bulk_store(&tmC0, fcol, y, abuf);
-            bulk_store(&tmC0, p.f + fcol, y, bbuf);
-            asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+          // da, db out with plain 16-byte stores (lane: 16-byte column q of token rows lane / 4 + 8 i),
+          // so the buffer pair is free as soon as the warp has read it: a TMA store would hold it
+          // until the SM's TMA unit, busy with the ring's loads, got round to reading it.
+          {
+            const int q = lane & 3;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              const int t = (lane >> 2) + 8 * i;
+              const uint32_t so = (uint32_t)t * 64 + ((uint32_t)(q ^ ((t >> 1) & 3)) << 4);
+              const uint4 va = ld_shared_v4(abuf + so), vb = ld_shared_v4(bbuf + so);
+              if (y + t < p.rows_max) {
+                __nv_bfloat16 *dst = p.out0 + (int64_t)(y + t) * p.ld0 + fcol + 8 * q;
+                *reinterpret_cast<uint4 *>(dst) = va;
+                *reinterpret_cast<uint4 *>(dst + p.f) = vb;
+              }
+            }
           }
-          issue_load(bi);   // the chunk two ahead reuses this buffer pair once its stores have read it
+          __syncwarp();
+          issue_load(bi);   // the chunk two ahead reuses this buffer pair
           __syncwarp();
           bi ^= 1;
         } else {   // DOWN, DGRAD
@@ -557,6 +581,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(G ? THREADS_G : THRE
       }
     }
     if (lane == 0) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+    if (K == DH) asm volatile("cp.async.wait_group 0;" ::: "memory");
     __syncwarp();
   }
 
@@ -696,6 +721,7 @@ int rows_dh(const void *dy, const void *wd, const void *ab, const int32_t *tile_
   p.f = f;
   p.out0 = (__nv_bfloat16 *)dab;
   p.ld0 = 2 * (int64_t)f;
+  p.in0 = (const __nv_bfloat16 *)ab;
   return launch<DH>(mA, mB, mC, mAB, p, (rows_max / 128) * p.n_ft, s);
 }
 

@@ -224,6 +224,16 @@ __device__ __forceinline__ void tmem_ld16x256b_x4(uint32_t taddr, uint32_t (&r)[
       : "r"(taddr));
 }
 
+// 16 bytes global -> shared through L2 (cp.async, generic proxy; completion by commit/wait groups).
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr) : "memory");
+  return v;
+}
+
 // Four 8x8 bf16 matrices in mma fragment layout (thread T: row T/4, columns 2 (T % 4) + {0, 1}),
 // stored transposed: row i of matrix m goes to the 16-byte shared-memory row whose address thread
 // 8m + i supplies, and holds column i of the fragment.
