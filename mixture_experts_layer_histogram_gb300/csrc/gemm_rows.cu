@@ -108,6 +108,7 @@ struct Params {
 // Tile = (expert e, token tile i, feature tile ft). Expert e's c rows fill n = ceil(c / 256) token
 // tiles: n - 1 full ones of 256 tokens, then the rest rounded up to a multiple of 32.
 struct Tile {
+  int index;      // position in the kernel's tile list
   int e, ft;
   int start;      // first grouped row of the tile
   int nt;         // tokens (the MMA's N): a multiple of 32, at most 256
@@ -115,33 +116,72 @@ struct Tile {
   bool ok;        // debug build: the tile passed its consistency checks (always true otherwise)
 };
 
-__device__ __forceinline__ Tile decode(int tile, const Params &p, const int *ttoff) {
-  Tile t;
-  const int gt = tile / p.n_ft;
-  t.ft = tile - gt * p.n_ft;
-  int lo = 0, hi = p.E - 1;   // last expert whose first token tile is <= gt (skips experts without rows)
-  while (lo < hi) {
-    const int mid = (lo + hi + 1) >> 1;
-    if (ttoff[mid] <= gt) lo = mid;
-    else hi = mid - 1;
+// One cluster's tiles in order: first, first + step, ... (tile = token tile gt * n_ft + feature
+// tile ft). Token tiles only grow along the walk, so each tile's expert (the last one whose first
+// token tile is <= gt; experts without rows are skipped) is found by stepping forward from the
+// previous tile's, and the division by n_ft happens once. The expert's offsets are loaded from
+// global memory one tile ahead, while the current tile runs: a tile boundary costs the ring only
+// the few shared-memory steps of the walk.
+struct TileWalker {
+  int tile, step, num_tiles;
+  int gt, ft, dgt, dft, e;
+  int o0, o1, g0, g1;   // offsets[e], offsets[e + 1], tile_offsets[e], tile_offsets[e + 1] of `tile`
+
+  __device__ __forceinline__ TileWalker(int first, int step_, int n, const Params &p, const int *ttoff)
+      : tile(first), step(step_), num_tiles(n) {
+    gt = first / p.n_ft;
+    ft = first - gt * p.n_ft;
+    dgt = step_ / p.n_ft;
+    dft = step_ - dgt * p.n_ft;
+    int lo = 0, hi = p.E - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (ttoff[mid] <= gt) lo = mid;
+      else hi = mid - 1;
+    }
+    e = lo;
+    load(p);
   }
-  t.e = lo;
-  const int i = gt - ttoff[lo];
-  const int c = p.offsets[lo + 1] - p.offsets[lo];
-  const int n = (c + NT_MAX - 1) / NT_MAX;
-  const bool last = i == n - 1;
-  t.nt = last ? ((c - NT_MAX * i + 31) & ~31) : NT_MAX;
-  t.start = p.tile_offsets[lo] * 128 + NT_MAX * i;
-  t.zero_end = last ? p.tile_offsets[lo + 1] * 128 : t.start + t.nt;
+  __device__ __forceinline__ void load(const Params &p) {
+    if (tile >= num_tiles) return;
+    o0 = p.offsets[e];
+    o1 = p.offsets[e + 1];
+    g0 = p.tile_offsets[e];
+    g1 = p.tile_offsets[e + 1];
+  }
+  // The walk's next tile into t; false past the last.
+  __device__ __forceinline__ bool next(Tile &t, const Params &p, const int *ttoff) {
+    if (tile >= num_tiles) return false;
+    t.index = tile;
+    t.e = e;
+    t.ft = ft;
+    const int i = gt - ttoff[e];
+    const int c = o1 - o0;
+    const int nt = (c + NT_MAX - 1) / NT_MAX;
+    const bool last = i == nt - 1;
+    t.nt = last ? ((c - NT_MAX * i + 31) & ~31) : NT_MAX;
+    t.start = g0 * 128 + NT_MAX * i;
+    t.zero_end = last ? g1 * 128 : t.start + t.nt;
 #if MOE_CHECKS
-  // the expert's routed rows fit its 128-row group, and the group lies inside the buffers
-  const int g0 = p.tile_offsets[lo], g1 = p.tile_offsets[lo + 1];
-  t.ok = c > 0 && g0 <= g1 && ((c + 31) & ~31) <= (g1 - g0) * 128 && (int64_t)g1 * 128 <= p.rows_max;
+    // the expert's routed rows fit its 128-row group, and the group lies inside the buffers
+    t.ok = c > 0 && g0 <= g1 && ((c + 31) & ~31) <= (g1 - g0) * 128 && (int64_t)g1 * 128 <= p.rows_max;
 #else
-  t.ok = true;
+    t.ok = true;
 #endif
-  return t;
-}
+    tile += step;
+    gt += dgt;
+    ft += dft;
+    if (ft >= p.n_ft) {
+      ft -= p.n_ft;
+      ++gt;
+    }
+    if (tile < num_tiles) {
+      while (e + 1 < p.E && ttoff[e + 1] <= gt) ++e;
+      load(p);
+    }
+    return true;
+  }
+};
 
 // Instruction descriptor, kind::f16: D fp32, A and B bf16, B K-major, A MN-major when a_mn,
 // M = 256 (the pair), N = nt.
@@ -250,10 +290,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(G ? THREADS_G : THRE
     // The whole warp runs the loop and waits, converged; one elected lane issues the copies.
     int stage = 0;
     uint32_t phase = 0;
-    for (int tile = cluster_id; tile < num_tiles; tile += num_clusters) {
-      const Tile t = decode(tile, p, ttoff);
+    TileWalker walk(cluster_id, num_clusters, num_tiles, p, ttoff);
+    for (Tile t; walk.next(t, p, ttoff);) {
       if (!t.ok) {   // debug build: every role skips the tile; the producer reports it
-        if (lane == 0) report(p.hdr, MOE_ERR_CHECK_FAILED, tile);
+        if (lane == 0) report(p.hdr, MOE_ERR_CHECK_FAILED, t.index);
         continue;
       }
       const int brow = t.start + (int)rank * (t.nt >> 1);   // this CTA's half of the tile's tokens
@@ -299,10 +339,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(G ? THREADS_G : THRE
     bool issued_any = false;
     const uint64_t desc_a0 = A_MN ? sdesc(sbase, C::BKP * 128, 1024) : sdesc(sbase, 16, 1024);
     const uint64_t desc_b0 = sdesc(sbase + C::A_BYTES, 16, 1024);
-    for (int tile = cluster_id; tile < num_tiles; tile += num_clusters) {
-      const Tile t = decode(tile, p, ttoff);
+    TileWalker walk(cluster_id, num_clusters, num_tiles, p, ttoff);
+    for (Tile t; walk.next(t, p, ttoff);) {
       if (!t.ok) continue;
-      if (!mbar_wait_cluster(tempty_bar(acc), acc_phase ^ 1u, abort_flag, p.hdr, 22)) break;
+      if (!mbar_ready_cluster(tempty_bar(acc), acc_phase ^ 1u) &&
+          !mbar_wait_cluster(tempty_bar(acc), acc_phase ^ 1u, abort_flag, p.hdr, 22))
+        break;
       tc_fence_after();
       const uint32_t d_tmem = tmem_base + (uint32_t)(acc * NT_MAX);
       const uint32_t id = idesc(A_MN, t.nt);
@@ -352,8 +394,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(G ? THREADS_G : THRE
     int fill = 0;                             // fills of the ring so far (all slots)
     uint32_t phase = 0;                       // parity of slot q's next fill
     bool ok = true;
-    for (int tile = cluster_id; tile < num_tiles && ok; tile += num_clusters) {
-      const Tile t = decode(tile, p, ttoff);
+    TileWalker walk(cluster_id, num_clusters, num_tiles, p, ttoff);
+    for (Tile t; ok && walk.next(t, p, ttoff);) {
       if (!t.ok) continue;
       const int brow = t.start + (int)rank * (t.nt >> 1), nrows = t.nt >> 1;
       int tok[16];
@@ -384,26 +426,25 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(G ? THREADS_G : THRE
     // DH: the saved a, b of a chunk arrive two chunks ahead into one of two buffer pairs, copied by
     // the warp itself with cp.async (one commit group per chunk): TMA copies would queue behind the
     // ring's loads in the SM's TMA unit, and the warp would stall issuing them.
-    int ltile = cluster_id, lj = hh;          // DH load cursor: next (tile, chunk) of this warp to bring in
+    // DH load cursor: chunk lj of tile lt is the next of this warp's chunks to bring in
+    TileWalker lwalk(cluster_id, num_clusters, num_tiles, p, ttoff);
     Tile lt{};
-    int lchunks = 0;
-    bool ldecoded = false;                    // lt describes ltile (decode reads global memory: once per tile)
+    int lj = hh, lchunks = 0;
+    bool lvalid = false;
+    if (K == DH) {
+      lvalid = lwalk.next(lt, p, ttoff);
+      lchunks = lvalid && lt.ok ? lt.nt >> 5 : 0;
+    }
     auto cursor_norm = [&]() {                // move the cursor to a chunk that exists
-      while (ltile < num_tiles) {
-        if (!ldecoded) {
-          lt = decode(ltile, p, ttoff);
-          lchunks = lt.ok ? lt.nt >> 5 : 0;
-          ldecoded = true;
-        }
-        if (lj < lchunks) return;
-        ltile += num_clusters;
+      while (lvalid && lj >= lchunks) {
+        lvalid = lwalk.next(lt, p, ttoff);
+        lchunks = lvalid && lt.ok ? lt.nt >> 5 : 0;
         lj = hh;
-        ldecoded = false;
       }
     };
     auto issue_load = [&](int b) {   // DH: one commit group, empty past the last chunk
       if (K != DH) return;
-      if (ltile < num_tiles) {
+      if (lvalid) {
         // lane: 16-byte column q of token rows lane / 4 + 8 i, into the 64-byte-swizzled layout
         const uint32_t dst = wbuf + (uint32_t)b * (2 * C::BUF_BYTES);
         const int x = lt.ft * 256 + (int)rank * 128 + quarter * 32, y = lt.start + 32 * lj, q = lane & 3;
@@ -429,8 +470,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(G ? THREADS_G : THRE
     }
     int acc = 0;
     uint32_t acc_phase = 0;
-    for (int tile = cluster_id; tile < num_tiles; tile += num_clusters) {
-      const Tile t = decode(tile, p, ttoff);
+    TileWalker walk(cluster_id, num_clusters, num_tiles, p, ttoff);
+    for (Tile t; walk.next(t, p, ttoff);) {
       if (!t.ok) continue;
       if (!mbar_wait_cluster(tfull_bar(acc), acc_phase, abort_flag, p.hdr, 24)) break;
       tc_fence_after();

@@ -441,28 +441,69 @@ __device__ __forceinline__ int snake_tile(int r, int c, int C, int num_tiles) {
   return s < num_tiles ? s : -1;
 }
 
-// The s-th weight-gradient tile in order of decreasing K (expert order[s / per], row pair, N tile)
-// as seen from CTA `rank`; t.kb counts ring stages of bkp rows.
-__device__ __forceinline__ Tile decode_wgrad(int s, const Params &p, const int *toff, const int *order, int rank,
-                                             int bkp) {
-  Tile t;
-  const int per = (p.m_tiles / 2) * p.n_tiles;
-  const int q = s / per;
-  t.e = order[q];
-  const int r = s - q * per;
-  t.m0 = (r / p.n_tiles) * (2 * BM) + rank * BM;
-  t.n0 = (r % p.n_tiles) * BN;
-  t.krow0 = toff[t.e] * BM;
-  t.kb = (toff[t.e + 1] - toff[t.e]) * (BM / bkp);
-#if MOE_CHECKS
-  // the expert's group is non-empty-or-empty in order, and the rows it reduces over lie inside the buffers
-  t.ok = toff[t.e] <= toff[t.e + 1] && (int64_t)toff[t.e + 1] * BM <= p.rows_max;
-  if (!t.ok) t.kb = 0;
-#else
-  t.ok = true;
-#endif
-  return t;
+// a / b for a >= 0 and b > 0, given rb = 1 / b in float: below 2^22 the float quotient is within
+// one of the true one; the remainder steps correct it (exactly, for any a).
+__device__ __forceinline__ int div_small(int a, int b, float rb) {
+  int q = __float2int_rz(__int2float_rn(a) * rb);
+  int r = a - q * b;
+  while (r < 0) {
+    --q;
+    r += b;
+  }
+  while (r >= b) {
+    ++q;
+    r -= b;
+  }
+  return q;
 }
+
+// The weight-gradient tiles a cluster runs, in its snake order, decoded one ahead: the expert's group
+// offsets are loaded from global memory while the previous tile runs, so a tile boundary costs the
+// ring only a few instructions. Tile s (in order of decreasing K) is expert order[s / per], row pair
+// and N tile of s % per, seen from CTA `rank`; t.kb counts ring stages of bkp rows.
+struct WgradWalker {
+  int r, cluster, clusters, num_tiles, per, rank, bkp;
+  float rper, rnt;
+  int s, e, k0, k1;   // the next tile and its expert's toff[e], toff[e + 1]
+  const int *toff, *order;
+
+  __device__ __forceinline__ WgradWalker(int cluster_, int clusters_, int num_tiles_, const Params &p,
+                                         const int *toff_, const int *order_, int rank_, int bkp_)
+      : r(0), cluster(cluster_), clusters(clusters_), num_tiles(num_tiles_), rank(rank_), bkp(bkp_), toff(toff_),
+        order(order_) {
+    per = (p.m_tiles / 2) * p.n_tiles;
+    rper = 1.0f / (float)per;
+    rnt = 1.0f / (float)p.n_tiles;
+    load();
+  }
+  __device__ __forceinline__ void load() {
+    s = snake_tile(r, cluster, clusters, num_tiles);
+    if (s < 0) return;
+    e = order[div_small(s, per, rper)];
+    k0 = toff[e];
+    k1 = toff[e + 1];
+  }
+  __device__ __forceinline__ bool next(Tile &t, const Params &p) {
+    if (s < 0) return false;
+    t.e = e;
+    const int q = s - div_small(s, per, rper) * per;
+    const int m = div_small(q, p.n_tiles, rnt);
+    t.m0 = m * (2 * BM) + rank * BM;
+    t.n0 = (q - m * p.n_tiles) * BN;
+    t.krow0 = k0 * BM;
+    t.kb = (k1 - k0) * (BM / bkp);
+#if MOE_CHECKS
+    // the expert's group is non-empty-or-empty in order, and the rows it reduces over lie inside the buffers
+    t.ok = k0 <= k1 && (int64_t)k1 * BM <= p.rows_max;
+    if (!t.ok) t.kb = 0;
+#else
+    t.ok = true;
+#endif
+    ++r;
+    load();
+    return true;
+  }
+};
 
 // G: B (x_perm for dW_gate_up) is gathered from x by token_of_row with cp.async by loader warps
 // instead of loaded by TMA (the permutation fused into the operand load): three sets of two warps,
@@ -541,8 +582,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(G ? THREADS + 32 * L
     // The whole warp runs the loop and waits, converged; one elected lane issues the copies.
     int stage = 0;
     uint32_t phase = 0;
-    for (int r = 0, tile; (tile = snake_tile(r, cluster_id, num_clusters, num_tiles)) >= 0; ++r) {
-      const Tile t = decode_wgrad(tile, p, toff, order, (int)rank, P_BK);
+    WgradWalker walk(cluster_id, num_clusters, num_tiles, p, toff, order, (int)rank, P_BK);
+    for (Tile t; walk.next(t, p);) {
       const int bn = t.n0 + (int)rank * (BN / 2);   // this CTA's half of B
       bool ok = true;
       for (int kb = 0; kb < t.kb; ++kb) {
@@ -575,10 +616,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(G ? THREADS + 32 * L
     bool issued_any = false;
     const uint64_t desc_a0 = sdesc(sbase, P_BK * 128, 1024);
     const uint64_t desc_b0 = sdesc(sbase + Cfg::A_BYTES, P_BK * 128, 1024);
-    for (int r = 0, tile; (tile = snake_tile(r, cluster_id, num_clusters, num_tiles)) >= 0; ++r) {
-      const Tile t = decode_wgrad(tile, p, toff, order, 0, P_BK);
+    WgradWalker walk(cluster_id, num_clusters, num_tiles, p, toff, order, 0, P_BK);
+    for (Tile t; walk.next(t, p);) {
       if (!t.ok || t.kb == 0) continue;
-      if (!mbar_wait_cluster(tempty_bar(acc), acc_phase ^ 1u, abort_flag, p.hdr, 12)) break;
+      if (!mbar_ready_cluster(tempty_bar(acc), acc_phase ^ 1u) &&
+          !mbar_wait_cluster(tempty_bar(acc), acc_phase ^ 1u, abort_flag, p.hdr, 12))
+        break;
       tc_fence_after();
       const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
       bool ok = true;
@@ -624,8 +667,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(G ? THREADS + 32 * L
     int fill = 0;
     uint32_t phase = 0;
     bool ok = true;
-    for (int r = 0, tile; ok && (tile = snake_tile(r, cluster_id, num_clusters, num_tiles)) >= 0; ++r) {
-      const Tile t = decode_wgrad(tile, p, toff, order, (int)rank, P_BK);
+    WgradWalker walk(cluster_id, num_clusters, num_tiles, p, toff, order, (int)rank, P_BK);
+    for (Tile t; ok && walk.next(t, p);) {
       if (!t.ok) continue;
       const int bn = t.n0 + (int)rank * (BN / 2);
       for (int kb = 0; kb < t.kb; ++kb, ++fill) {
@@ -652,8 +695,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(G ? THREADS + 32 * L
     EpiStore es{smem_u32(epi_smem) + (uint32_t)(warp - 2) * 2 * EPI_BUF_BYTES, 0, lane};
     int acc = 0;
     uint32_t acc_phase = 0;
-    for (int r = 0, tile; (tile = snake_tile(r, cluster_id, num_clusters, num_tiles)) >= 0; ++r) {
-      const Tile t = decode_wgrad(tile, p, toff, order, (int)rank, P_BK);
+    WgradWalker walk(cluster_id, num_clusters, num_tiles, p, toff, order, (int)rank, P_BK);
+    for (Tile t; walk.next(t, p);) {
       if (!t.ok) continue;
       if (t.kb == 0) {   // an expert with no rows: its gradient is zero
         __nv_bfloat16 *dst =

@@ -147,6 +147,18 @@ static __device__ __noinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t par
     }
   }
 }
+// One non-blocking look (cluster-scope acquire): true when the phase with parity `parity` is done.
+__device__ __forceinline__ bool mbar_ready_cluster(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
 // The same bounded wait, polling with mbarrier.test_wait, which never suspends the thread. For the
 // two roles of the pair GEMMs' rings (the TMA producer and the MMA issuer, each a converged warp): a
 // phase that completes is seen a little sooner than through try_wait's suspend-and-wake, which
