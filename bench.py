@@ -26,6 +26,7 @@ from __future__ import annotations
 import argparse
 import json
 import os
+import math
 import statistics
 import subprocess
 import sys
@@ -43,7 +44,7 @@ METRIC_FWD = "MoE layer fwd tokens/s (E=64,k=8,d=2048); grouped-GEMM % BF16 peak
 # kernel changes, its traffic is unmeasured (null) until it is captured again.
 GEMM_SOURCES = ("gemm_tc.cu", "tc_ptx.cuh", "tma_host.cuh", "common.cuh")
 GEMM_TRAFFIC = {    # workload -> (bytes per step, source digest)
-    "fwdbwd_t8192": (5749641216, "3a5a0679444d39a6"),
+    "fwdbwd_t8192": (5782926336, "763975cb0c394517"),
 }
 DEFAULT_WORKLOAD = "fwdbwd_t8192"
 
@@ -281,7 +282,10 @@ def run_ours(args):
     elapsed_ms = max_over_ranks(t_start.elapsed_time(t_end), world, dev)
     # per-kernel times: a second pass of eager steps, each C-ABI call between two events on the
     # stream its kernels are launched on (the roofline's achieved rate comes from these)
-    nper = max(3, min(args.steps, args.kernel_steps))
+    if args.kernel_steps is None:
+        nper = min(2000, max(50, math.ceil(400.0 / max(elapsed_ms / max(args.steps, 1), 1e-3))))
+    else:
+        nper = max(3, min(args.steps, args.kernel_steps))
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(10)] for _ in range(nper)]
     torch.cuda.synchronize(dev)
     k0 = time.time()
@@ -487,8 +491,9 @@ def main():
     ap.add_argument("--recompute", action="store_true",
                     help="backward recomputes ab, h from x_perm (selective activation checkpointing)")
     ap.add_argument("--ref-tokens", type=int, default=8)
-    ap.add_argument("--kernel-steps", type=int, default=50,
-                    help="eager steps of the separate per-kernel timing pass (at most --steps)")
+    ap.add_argument("--kernel-steps", type=int, default=None,
+                    help="eager steps of the separate per-kernel timing pass (default: enough for 0.4 s, at "
+                         "least 50, so that the clock sampler sees the kernels run)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("at least 3 warm-up steps")
