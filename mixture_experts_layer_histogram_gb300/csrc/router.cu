@@ -161,8 +161,10 @@ __global__ void __launch_bounds__(R_THREADS, 1)
   tc_fence_after();
   const uint32_t tmem_base = *tmem_holder;
 
-  if (warp == 0 && lane == 0) {
+  if (warp == 0) {
     // ------------------------------------------------------------------ TMA producer
+    // The whole warp runs the loop and polls the ring, converged; one elected lane issues. Each
+    // stage carries little tensor work here, so the hand-off per stage sets the kernel's pace.
     int stage = 0;
     uint32_t phase = 0, issued = 0;
     bool ok = true;
@@ -170,12 +172,15 @@ __global__ void __launch_bounds__(R_THREADS, 1)
       const int tile = u / splits, kb0 = (u - tile * splits) * p.kb_split;
       const int kb1 = min(p.num_kb, kb0 + p.kb_split);
       for (int kb = kb0; kb < kb1; ++kb) {
-        if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag, p.hdr, 11)) { ok = false; break; }
-        const uint32_t sA = sbase + stage * p.stage_bytes, fb = full_bar(stage);
-        mbar_expect_tx(fb, p.stage_bytes);
+        if (!mbar_spin_cluster(empty_bar(stage), phase ^ 1u, abort_flag, p.hdr, 11)) { ok = false; break; }
+        if (elect_one()) {
+          const uint32_t sA = sbase + stage * p.stage_bytes, fb = full_bar(stage);
+          mbar_expect_tx(fb, p.stage_bytes);
+          tma_load_2d(sA, &tmX, kb * RBK, tile * RBM, fb);
+          tma_load_2d(sA + R_A_BYTES, &tmW, kb * RBK, 0, fb);
+        }
+        __syncwarp();
         issued |= 1u << stage;
-        tma_load_2d(sA, &tmX, kb * RBK, tile * RBM, fb);
-        tma_load_2d(sA + R_A_BYTES, &tmW, kb * RBK, 0, fb);
         if (++stage == S) { stage = 0; phase ^= 1u; }
       }
     }
@@ -185,11 +190,14 @@ __global__ void __launch_bounds__(R_THREADS, 1)
       const uint64_t t0 = global_ns();
       while (!mbar_try_wait(full_bar(s), ph) && global_ns() - t0 < kWaitLimitNs) {}
     }
-  } else if (warp == 1 && lane == 0) {
+  } else if (warp == 1) {
     // ------------------------------------------------------------------ MMA issuer
-    // kind::f16, D fp32, A and B bf16 K-major, M = 128, N = n_mma
+    // kind::f16, D fp32, A and B bf16 K-major, M = 128, N = n_mma. The whole warp polls, one
+    // elected lane issues; the descriptors are formed once (shared-memory addresses below 256 KB:
+    // a stage's or k step's offset adds to the start-address field without carry).
     const uint32_t idesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(p.n_mma >> 3) << 17) |
                            ((uint32_t)(RBM >> 4) << 24);
+    const uint64_t desc_a0 = sdesc(sbase, 16, 1024), desc_b0 = sdesc(sbase + R_A_BYTES, 16, 1024);
     int stage = 0, acc = 0;
     uint32_t phase = 0, acc_phase = 0;
     bool issued_any = false, ok = true;
@@ -200,24 +208,29 @@ __global__ void __launch_bounds__(R_THREADS, 1)
       tc_fence_after();
       const uint32_t d_tmem = tmem_base + (uint32_t)(acc * p.acc_cols);
       for (int kb = kb0; kb < kb1; ++kb) {
-        if (!mbar_wait(full_bar(stage), phase, abort_flag, p.hdr, 13)) { ok = false; break; }
+        if (!mbar_spin_cluster(full_bar(stage), phase, abort_flag, p.hdr, 13)) { ok = false; break; }
         tc_fence_after();
-        const uint32_t sA = sbase + stage * p.stage_bytes, sB = sA + R_A_BYTES;
+        if (elect_one()) {
+          const uint32_t so = (uint32_t)(stage * p.stage_bytes) >> 4;
 #pragma unroll
-        for (int kk = 0; kk < RBK / 16; ++kk)
-          mma_bf16(d_tmem, sdesc(sA + kk * 32, 16, 1024), sdesc(sB + kk * 32, 16, 1024), idesc,
-                   (kb != kb0 || kk != 0) ? 1u : 0u);
+          for (int kk = 0; kk < RBK / 16; ++kk)
+            mma_bf16(d_tmem, desc_a0 + so + (uint32_t)(kk * 2), desc_b0 + so + (uint32_t)(kk * 2), idesc,
+                     (kb != kb0 || kk != 0) ? 1u : 0u);
+          mma_commit(empty_bar(stage));
+        }
+        __syncwarp();
         issued_any = true;
-        mma_commit(empty_bar(stage));
         if (++stage == S) { stage = 0; phase ^= 1u; }
       }
       if (!ok) break;
-      mma_commit(tfull_bar(acc));
+      if (elect_one()) mma_commit(tfull_bar(acc));
+      __syncwarp();
       acc ^= 1;
       if (acc == 0) acc_phase ^= 1u;
     }
     if (issued_any) {
-      mma_commit(mma_done_bar);
+      if (elect_one()) mma_commit(mma_done_bar);
+      __syncwarp();
       const uint64_t t0 = global_ns();
       while (!mbar_try_wait(mma_done_bar, 0) && global_ns() - t0 < kWaitLimitNs) {}
     }
