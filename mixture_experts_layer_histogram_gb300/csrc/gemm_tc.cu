@@ -275,8 +275,9 @@ __global__ void __launch_bounds__(THREADS, 1)
 
   const int num_tiles = row_reduce(KIND) ? p.E * p.m_tiles * p.n_tiles : toff[p.E] * p.n_tiles;
 
-  if (warp == 0 && lane == 0) {
+  if (warp == 0) {
     // ------------------------------------------------------------------ TMA producer
+    // The whole warp runs the loop and polls the ring, converged; one elected lane issues.
     int stage = 0;
     uint32_t phase = 0;
     uint32_t issued = 0;   // bit s: stage s has a load whose completion nobody has waited for yet
@@ -284,21 +285,24 @@ __global__ void __launch_bounds__(THREADS, 1)
       const Tile t = decode<KIND>(tile, p, toff);
       bool ok = true;
       for (int kb = 0; kb < t.kb; ++kb) {
-        if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag, p.hdr, 1)) { ok = false; break; }
-        const uint32_t sA = sbase + stage * STAGE_BYTES, sB = sA + A_BYTES, fb = full_bar(stage);
-        mbar_expect_tx(fb, STAGE_BYTES);
-        issued |= 1u << stage;
-        const int kx = kb * BK;
-        if (KIND == RDX) {   // K-major A (dL rows), MN-major B (Wr; rows past E read as zero)
-          tma_load_2d(sA, &tmA, kx, t.m0, fb);
+        if (!mbar_spin_cluster(empty_bar(stage), phase ^ 1u, abort_flag, p.hdr, 1)) { ok = false; break; }
+        if (elect_one()) {
+          const uint32_t sA = sbase + stage * STAGE_BYTES, sB = sA + A_BYTES, fb = full_bar(stage);
+          mbar_expect_tx(fb, STAGE_BYTES);
+          const int kx = kb * BK;
+          if (KIND == RDX) {   // K-major A (dL rows), MN-major B (Wr; rows past E read as zero)
+            tma_load_2d(sA, &tmA, kx, t.m0, fb);
 #pragma unroll
-          for (int q = 0; q < BN / 64; ++q) tma_load_2d(sB + q * 8192, &tmB, t.n0 + 64 * q, kx, fb);
-        } else {   // RDW
+            for (int q = 0; q < BN / 64; ++q) tma_load_2d(sB + q * 8192, &tmB, t.n0 + 64 * q, kx, fb);
+          } else {   // RDW
 #pragma unroll
-          for (int q = 0; q < BM / 64; ++q) tma_load_2d(sA + q * 8192, &tmA, t.m0 + 64 * q, t.krow0 + kx, fb);
+            for (int q = 0; q < BM / 64; ++q) tma_load_2d(sA + q * 8192, &tmA, t.m0 + 64 * q, t.krow0 + kx, fb);
 #pragma unroll
-          for (int q = 0; q < BN / 64; ++q) tma_load_2d(sB + q * 8192, &tmB, t.n0 + 64 * q, t.krow0 + kx, fb);
+            for (int q = 0; q < BN / 64; ++q) tma_load_2d(sB + q * 8192, &tmB, t.n0 + 64 * q, t.krow0 + kx, fb);
+          }
         }
+        __syncwarp();
+        issued |= 1u << stage;
         if (++stage == STAGES) { stage = 0; phase ^= 1u; }
       }
       if (!ok) break;
@@ -312,12 +316,16 @@ __global__ void __launch_bounds__(THREADS, 1)
       const uint64_t t0 = global_ns();
       while (!mbar_try_wait(full_bar(s), ph) && global_ns() - t0 < kWaitLimitNs) {}
     }
-  } else if (warp == 1 && lane == 0) {
+  } else if (warp == 1) {
     // ------------------------------------------------------------------ MMA issuer
+    // The whole warp polls, one elected lane issues; the descriptors are formed once
+    // (shared-memory addresses below 256 KB: an offset adds to the start-address field without carry).
     constexpr uint32_t idesc = idesc_bf16(A_MN, B_MN);
     int stage = 0, acc = 0;
     uint32_t phase = 0, acc_phase = 0;
     bool issued_any = false;
+    const uint64_t desc_a0 = A_MN ? sdesc(sbase, 8192, 1024) : sdesc(sbase, 16, 1024);
+    const uint64_t desc_b0 = B_MN ? sdesc(sbase + A_BYTES, 8192, 1024) : sdesc(sbase + A_BYTES, 16, 1024);
     for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
       const Tile t = decode<KIND>(tile, p, toff);
       if (t.kb == 0) continue;
@@ -326,26 +334,31 @@ __global__ void __launch_bounds__(THREADS, 1)
       const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
       bool ok = true;
       for (int kb = 0; kb < t.kb; ++kb) {
-        if (!mbar_wait(full_bar(stage), phase, abort_flag, p.hdr, 3)) { ok = false; break; }
+        if (!mbar_spin_cluster(full_bar(stage), phase, abort_flag, p.hdr, 3)) { ok = false; break; }
         tc_fence_after();
-        const uint32_t sA = sbase + stage * STAGE_BYTES, sB = sA + A_BYTES;
+        if (elect_one()) {
+          const uint32_t so = (uint32_t)(stage * STAGE_BYTES) >> 4;
 #pragma unroll
-        for (int kk = 0; kk < BK / 16; ++kk) {
-          const uint64_t ad = A_MN ? sdesc(sA + kk * 2048, 8192, 1024) : sdesc(sA + kk * 32, 16, 1024);
-          const uint64_t bd = B_MN ? sdesc(sB + kk * 2048, 8192, 1024) : sdesc(sB + kk * 32, 16, 1024);
-          mma_bf16(d_tmem, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
+          for (int kk = 0; kk < BK / 16; ++kk) {
+            const uint32_t ka = A_MN ? (uint32_t)(kk * 2048 >> 4) : (uint32_t)(kk * 32 >> 4);
+            const uint32_t kb_ = B_MN ? (uint32_t)(kk * 2048 >> 4) : (uint32_t)(kk * 32 >> 4);
+            mma_bf16(d_tmem, desc_a0 + so + ka, desc_b0 + so + kb_, idesc, (kb | kk) != 0 ? 1u : 0u);
+          }
+          mma_commit(empty_bar(stage));   // frees the smem stage once these MMAs have read it
         }
+        __syncwarp();
         issued_any = true;
-        mma_commit(empty_bar(stage));   // frees the smem stage once these MMAs have read it
         if (++stage == STAGES) { stage = 0; phase ^= 1u; }
       }
       if (!ok) break;
-      mma_commit(tfull_bar(acc));       // accumulator ready for the epilogue
+      if (elect_one()) mma_commit(tfull_bar(acc));   // accumulator ready for the epilogue
+      __syncwarp();
       acc ^= 1;
       if (acc == 0) acc_phase ^= 1u;
     }
     if (issued_any) {   // every MMA must have completed before TMEM is released
-      mma_commit(mma_done_bar);
+      if (elect_one()) mma_commit(mma_done_bar);
+      __syncwarp();
       const uint64_t t0 = global_ns();
       while (!mbar_try_wait(mma_done_bar, 0) && global_ns() - t0 < kWaitLimitNs) {}
     }
