@@ -28,6 +28,10 @@ CASES = [
     (4, 512, 256, [1024, 1, 640, 897]),
     (5, 256, 256, [257, 31, 32, 33, 2049]),
     (1, 768, 256, [4095]),
+    # The schedulers walk each cluster's tiles by stepping forward over the experts: long runs of
+    # empty experts between tiles, and many one-tile experts (each cluster steps over several).
+    (64, 256, 256, [0] * 20 + [300] + [0] * 10 + [1] + [0] * 5 + [700] + [0] * 26),
+    (256, 256, 256, [1 + (e * 7) % 5 for e in range(256)]),
 ]
 
 
