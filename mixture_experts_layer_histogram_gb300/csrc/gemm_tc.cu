@@ -153,6 +153,34 @@ struct EpiStore {
     }
     bi ^= 1;
   }
+  // The same 32 x 32 block written with plain 16-byte stores from the staging buffer (four lanes per
+  // 64-byte row, eight rows per instruction): block row i goes to out + (y + i) ld + x. In the
+  // weight-gradient kernel TMA stores queued with the ring's operand loads in the SM's TMA unit and
+  // left the MMA waiting for data; these stores do not.
+  __device__ __forceinline__ void put_plain(__nv_bfloat16 *out, int64_t ld, int x, int y, const float *v) {
+    const uint32_t b = buf;
+    const uint32_t row = b + (uint32_t)lane * 64, sw = (uint32_t)(lane >> 1) & 3u;
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      const uint4 q = pack_bf16x8(v + 8 * c);
+      asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(row + ((c ^ sw) << 4)), "r"(q.x), "r"(q.y), "r"(q.z),
+                   "r"(q.w)
+                   : "memory");
+    }
+    __syncwarp();
+    const int q = lane & 3;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int rr = (lane >> 2) + 8 * i;
+      uint4 val;
+      asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                   : "=r"(val.x), "=r"(val.y), "=r"(val.z), "=r"(val.w)
+                   : "r"(b + (uint32_t)rr * 64 + (((uint32_t)q ^ (((uint32_t)rr >> 1) & 3u)) << 4))
+                   : "memory");
+      *reinterpret_cast<uint4 *>(out + (int64_t)(y + rr) * ld + x + 8 * q) = val;
+    }
+    __syncwarp();   // the buffer is rewritten by the next block
+  }
   __device__ __forceinline__ void drain() {
     if (lane == 0) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
     __syncwarp();
@@ -182,15 +210,6 @@ __device__ __forceinline__ void epilogue_tile(const Tile &t, const Params &p, ui
                 make_float4(__uint_as_float(r[4 * q]), __uint_as_float(r[4 * q + 1]), __uint_as_float(r[4 * q + 2]),
                             __uint_as_float(r[4 * q + 3]));
       }
-    }
-  } else if constexpr (KIND != RDX) {
-#pragma unroll 1
-    for (int c = c0; c < c0 + BN / 2; c += 32) {
-      tmem_ld32(tbase + c, r);
-      tmem_ld_wait();
-#pragma unroll
-      for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
-      es.put(mc0, t.n0 + c, yrow, v);
     }
   } else {
     // RDX: with an addend, this row's previous dx, loaded in full (pre) before the accumulator was
@@ -722,7 +741,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(G ? THREADS + 32 * L
       if (!mbar_wait_cluster(tfull_bar(acc), acc_phase, abort_flag, p.hdr, 14)) break;
       tc_fence_after();
       const uint32_t tbase = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * BN);
-      epilogue_tile<WGRAD>(t, p, tbase, row_in_tile, epi_yrow<WGRAD>(t, p, quarter), c0, pre, es, &tmC0);
+      {   // dW blocks through the staging buffer with plain coalesced stores (see put_plain)
+        const int yrow = epi_yrow<WGRAD>(t, p, quarter);
+#pragma unroll 1
+        for (int c = c0; c < c0 + BN / 2; c += 32) {
+          uint32_t r[32];
+          tmem_ld32(tbase + c, r);
+          tmem_ld_wait();
+          float v[32];
+#pragma unroll
+          for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+          es.put_plain(p.out0, p.ld0, t.n0 + c, yrow, v);
+        }
+        (void)pre;
+      }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive_cluster(mapa_shared(tempty_bar(acc), 0));
