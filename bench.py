@@ -379,7 +379,10 @@ def run_ours(args):
                                           if peaks.get("bf16_sustained") else None),
                     "kernel_clocks": kclk,
                     "kernel_times": f"events around each C-ABI call, {nper} eager steps after the timed region",
-                    "algorithmic_flop_per_step": gemm_flop, "traffic": gemm_traffic(w.name),
+                    "algorithmic_flop_per_step": gemm_flop,
+                    # the stored capture is of the plain pass's six GEMM launches; a gathering or a
+                    # recomputing pass runs other ones
+                    "traffic": None if (args.gather or args.recompute) else gemm_traffic(w.name),
                     "traffic_unit": "DRAM bytes per step (all grouped-GEMM launches)"}
     else:   # true-fp32 FFMA path: bound by the FP32 pipes (152 SMs x 128 lanes x 2 FLOP x 2.07 GHz)
         fp32_peak = 152 * 128 * 2 * 2.07e9 / 1e12
