@@ -18,8 +18,8 @@
 // ones of 256 tokens, then the rest rounded up to a multiple of 32, so the pair computes at most 31
 // rows past an expert's last token: no discarded tile, no padding beyond the next multiple of 32.
 // The tile count is the same as with tokens as A (ceil(ceil(c_e / 128) / 2) = ceil(c_e / 256)
-// pairs), and a tile's time is set mostly by its ring stages (one per 128 of K), not by its N, so
-// the gain is the tensor work (and power) of the rows no longer computed, plus a cheaper epilogue.
+// pairs), and a tile's time is set mostly by its ring stages, not by its N, so the gain is the
+// tensor work (and power) of the rows no longer computed, plus a cheaper epilogue.
 // Every tile loads full 128-row token boxes: loading only the rows a short tile uses took more,
 // smaller TMA requests and was slower.
 //
@@ -27,17 +27,21 @@
 // column = token. The epilogue reads it with tcgen05.ld.16x256b, whose register layout is that of
 // an mma fragment (thread T: lanes T/4 and T/4 + 8, columns 2 (T % 4) + {0, 1}), converts to bf16
 // and writes token-major blocks to shared memory with stmatrix .trans; a TMA bulk tensor store
-// writes each block out. DH reads its saved a, b blocks the same way round (TMA load, then
-// ldmatrix .trans). GATEUP's A holds each group of 8 gate rows next to the same features' 8 up
+// writes each block out. DH works the other way round as well: it copies its saved a, b blocks in
+// with cp.async and ldmatrix .trans, and writes da, db with plain coalesced stores (its TMA copies
+// queued behind the ring's loads in the SM's TMA unit). GATEUP's A holds each group of 8 gate rows next to the same features' 8 up
 // rows (a 5D tensor map), so one thread receives a (lane T/4) and b (lane T/4 + 8) of the same
 // feature and token and computes h in registers.
 //
 // Warp roles per CTA (both CTAs of the pair):
 //   warp 0      TMA producer: 128 weight rows and 128 token rows per k-block into a shared-memory
-//               ring (three 128-deep stages; DH five 64-deep stages, its epilogue buffers take the
-//               rest)
+//               ring of six 64-deep stages (DH five: its epilogue buffers take the sixth); the whole
+//               warp polls the ring, one elected lane issues
 //   warp 1      TMEM allocation (512 columns, two accumulators of up to 256 tokens); in the leader
-//               CTA one thread issues the MMAs and commits to both CTAs' barriers
+//               CTA the converged warp issues the MMAs from one elected lane and commits to both
+//               CTAs' barriers
+// Each role walks the cluster's tiles incrementally (TileWalker): no division or search at a tile
+// boundary, the next tile's offsets loaded while the current one runs.
 //   warps 2..9  epilogue: two warps per 32-lane TMEM quarter, each taking every second 32-token chunk
 // Padding rows (from the last computed token of an expert up to its group's multiple of 128) are
 // written with zeros by the expert's last tile. Every wait is bounded (0.2 s): on timeout the kernel
@@ -68,6 +72,7 @@ constexpr int MAX_E = MOE_MAX_EXPERTS;
 // The ring: 64-deep stages, as many as fit beside the epilogue's staging buffers (a load's latency
 // under full load is about as long for a 32 KB stage as for a 64 KB one, so more, smaller stages
 // keep more of it covered). Gathering GATEUP (G) keeps three 128-deep stages, one per loader set.
+// (Deeper rings for the gathering kind measured no faster: its loaders set its pace.)
 template <int K, bool G = false> struct Cfg {
   static constexpr int BKP = G ? 128 : 64;                   // k depth of one ring stage
   static constexpr int KA = BKP / 64;                        // 128-byte swizzle atoms along k per stage

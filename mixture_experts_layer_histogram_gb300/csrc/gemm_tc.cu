@@ -9,14 +9,17 @@
 //   WGRAD   dW[e] = act1_e^T act2_e over expert e's rows (A and B read MN-major, K = the expert's
 //           padded row count; experts without rows get zero gradients without touching TMEM), on
 //           the CTA-pair kernel (tcgen05.mma.cta_group::2, 256 x 256 tiles, the pairs run along the
-//           weight rows, three 128-deep ring stages)
+//           weight rows, six 64-deep ring stages; the epilogue writes dW with plain coalesced
+//           stores from a staging buffer)
 //   RDX     dx (+)= dL Wr (B read MN-major; the epilogue adds the previous dx when asked), and
 //   RDW     fp32 partial dWr = dL_g^T x_g over token range g (A and B MN-major), plain fp32 stores,
 //           the router backward's two kinds, on the single-CTA kernel (one "group" = all tokens for
 //           RDX, one token range per group for RDW):
 //
-//   warp 0      TMA producer: 128B-swizzled tiles of A and B into a shared-memory ring
-//   warp 1      allocates the 512 TMEM columns, issues tcgen05.mma (one thread), commits to barriers
+//   warp 0      TMA producer: 128B-swizzled tiles of A and B into a shared-memory ring (the whole
+//               warp polls, one elected lane issues)
+//   warp 1      allocates the 512 TMEM columns, issues tcgen05.mma from one elected lane of the
+//               converged warp, commits to barriers
 //   warps 2..9  epilogue: tcgen05.ld of the fp32 accumulator (double-buffered in TMEM, 2 x 256
 //               columns) -> bf16 or fp32 -> global; two warps share each 32-lane TMEM quarter and
 //               take one half of the tile's columns each
