@@ -120,9 +120,10 @@ int moe_count_index(const int32_t *topk_idx, int T, int k, int E, int32_t *count
  * Routing, token counting and index generation in one launch (brief, section 核心方法: expert
  * selection feeding the GPU kernels for token counting and index generation): the results of
  * moe_route_topk followed by moe_count_index, bit for bit (topk_idx, topk_w, counts, offsets,
- * tile_offsets, row_of_slot, token_of_row), from one kernel that routes a block's tokens, ranks
- * its slots, publishes its counts and look-back aggregates, and scatters once the last block has
- * scanned the totals. Arguments, shapes, workspace size and device errors are those of the two
+ * tile_offsets, row_of_slot, token_of_row), from one kernel whose blocks route their tokens, rank
+ * their slots and publish their per-expert counts; once every block has published (a bounded wait
+ * of about 0.2 s), each block scans the totals, sums its predecessors' counts and scatters.
+ * Arguments, shapes, workspace size and device errors are those of the two
  * calls (the selection cannot produce an expert id outside [0, E)); the look-back fault hook is not
  * read and is cleared. The blocks wait for one another, so the kernel runs only when all of them
  * fit on the GPU at once (T*k up to about 300K slots on a GB300); above that the call makes the

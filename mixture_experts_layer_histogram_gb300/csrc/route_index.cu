@@ -11,8 +11,9 @@
 //                  look-back over the preceding blocks (one 64-bit flag|value word per block and
 //                  expert), and scatters row_of_slot / token_of_row.
 //   route_count_index kernel : the routing, count and index kernels' work in one launch (each block
-//                  routes the tokens of its slots, then ranks, counts, looks back and scatters; the
-//                  blocks meet once, at the last block's scan of the totals).
+//                  routes the tokens of its slots, two lanes per token, ranks its slots and publishes
+//                  its per-expert counts; the blocks meet once, when all have published, and then each
+//                  block scans the totals and sums its predecessors' counts itself and scatters).
 #include <math.h>
 
 #include "common.cuh"
@@ -307,103 +308,238 @@ __global__ void __launch_bounds__(kIdxThreads) index_kernel(const int32_t *__res
 
 // ---------------------------------------------------------------------------------------------
 // Routing, counting and index generation in one kernel (moe_route_count_index). Block b owns the
-// same kIdxChunk slots as index_kernel's block b. It routes the tokens those slots belong to (a
-// token whose slots straddle two blocks is routed by both, with identical results; the block
-// holding its first slot writes topk_idx / topk_w), ranks its slots stably per expert, adds its
-// counts to the global totals and publishes its look-back aggregate. The last block to do so
-// computes the scans (counts, offsets, tile_offsets) and raises a flag; meanwhile every block looks
-// back over its predecessors, then waits for the flag (bounded, about 0.2 s) and scatters. The
-// wait needs every block resident at once: the host launches this kernel cooperatively, and only
-// when the whole grid fits on the GPU.
+// same kIdxChunk slots as index_kernel's block b.
+//   1. Routing: each token of the block's slots is routed by a pair of adjacent lanes, each lane
+//      keeping the top-k of one half of the experts; the lower lane merges the upper lane's list
+//      into its own (route_token_pair). A token whose slots straddle two blocks is routed by both,
+//      identically; the block holding its first slot writes topk_idx / topk_w.
+//   2. Ranks: warp w owns slots [w*128, w*128+128) of the chunk, four rounds of 32; a slot's rank
+//      within its expert is the warp's running count (match.any per round, no block barrier),
+//      plus the slots of that expert in the block's earlier warps.
+//   3. The block publishes its per-expert counts (one row of agg) and adds them to the totals acc,
+//      then counts itself in. Once all blocks have (a bounded wait of about 0.2 s), every block
+//      reads the totals and its predecessors' rows from L2, scans the totals itself, and scatters
+//      row_of_slot / token_of_row; block 0 writes counts, offsets and tile_offsets.
+// The blocks wait for one another, so all of them must be resident at once: the host launches the
+// kernel cooperatively, and only when the whole grid fits on the GPU.
+template <int KMAX>
+__device__ __forceinline__ void route_token_pair(const float *__restrict__ logits, int64_t t, bool active, int E,
+                                                 int k, int (&ti)[KMAX], float (&w)[KMAX]) {
+  const int h = threadIdx.x & 1;
+  const int split = min(E, ((E + 1) / 2 + 3) & ~3);   // the upper half starts on a 16-byte boundary
+  const int lo = h ? split : 0, hi = h ? E : split;
+  const float *row = logits + t * E;
+  const bool vec = (E & 3) == 0;
+  float tv[KMAX];
+#pragma unroll
+  for (int j = 0; j < KMAX; ++j) {
+    tv[j] = -INFINITY;
+    ti[j] = 0;
+  }
+  if (active) {
+    for (int e0 = lo; e0 < hi; e0 += 64) {
+      float v[64];
+      if (vec) {
+#pragma unroll
+        for (int q = 0; q < 16; ++q) {
+          const float4 f = e0 + 4 * q < hi ? __ldg(reinterpret_cast<const float4 *>(row + e0) + q)
+                                           : make_float4(0.f, 0.f, 0.f, 0.f);
+          v[4 * q] = f.x;
+          v[4 * q + 1] = f.y;
+          v[4 * q + 2] = f.z;
+          v[4 * q + 3] = f.w;
+        }
+      } else {
+#pragma unroll
+        for (int i = 0; i < 64; ++i) v[i] = e0 + i < hi ? __ldg(row + e0 + i) : 0.0f;
+      }
+#pragma unroll
+      for (int i = 0; i < 64; ++i)
+        if (e0 + i < hi) topk_insert<KMAX>(tv, ti, v[i], e0 + i);
+    }
+  }
+  // The upper lane's entries all carry higher ids than the lower lane's and arrive in their list
+  // order (value desc, id asc), which is the order topk_insert requires.
+#pragma unroll
+  for (int j = 0; j < KMAX; ++j) {
+    const float pv = __shfl_xor_sync(0xffffffffu, tv[j], 1);
+    const int pi = __shfl_xor_sync(0xffffffffu, ti[j], 1);
+    if (h == 0 && j < k) topk_insert<KMAX>(tv, ti, pv, pi);
+  }
+  const float m = tv[0];
+  float s = 0.0f;
+#pragma unroll
+  for (int j = 0; j < KMAX; ++j) {
+    w[j] = j < k ? expf(tv[j] - m) : 0.0f;
+    s += w[j];
+  }
+#pragma unroll
+  for (int j = 0; j < KMAX; ++j) w[j] = w[j] / s;
+}
+
 template <int KMAX>
 __global__ void __launch_bounds__(kIdxThreads) route_count_index_kernel(
     const float *__restrict__ logits, int T, int E, int k, int BM, WsHeader *hdr, int32_t *acc,
-    uint64_t *__restrict__ lookback, int32_t *__restrict__ topk_idx, float *__restrict__ topk_w, int32_t *counts,
-    int32_t *offsets, int32_t *tile_offsets, int32_t *__restrict__ row_of_slot, int32_t *__restrict__ token_of_row) {
-  __shared__ int sk[kIdxChunk];                       // experts of this block's slots, slot order
-  __shared__ int warp_cnt[kIdxThreads / 32][MOE_MAX_EXPERTS];
-  __shared__ int run[MOE_MAX_EXPERTS];
-  __shared__ int excl[MOE_MAX_EXPERTS];
-  __shared__ int row_base[MOE_MAX_EXPERTS];
-  __shared__ int bid_s;
-  __shared__ bool is_last, ready;
-  const int tid = threadIdx.x;
-  if (tid == 0) bid_s = (int)atomicAdd(&hdr->tickets[1], 1u);
-  for (int i = tid; i < (kIdxThreads / 32) * MOE_MAX_EXPERTS; i += kIdxThreads) (&warp_cnt[0][0])[i] = 0;
-  for (int e = tid; e < E; e += kIdxThreads) run[e] = 0;
-  __syncthreads();
-  const int b = bid_s;
+    int32_t *agg, int32_t *__restrict__ topk_idx, float *__restrict__ topk_w, int32_t *__restrict__ counts,
+    int32_t *__restrict__ offsets, int32_t *__restrict__ tile_offsets, int32_t *__restrict__ row_of_slot,
+    int32_t *__restrict__ token_of_row) {
+  constexpr int kWarps = kIdxThreads / 32, kWarpSlots = 32 * kIdxItems;
+  __shared__ int sk[kIdxChunk];                            // experts of this block's slots, slot order
+  __shared__ int warp_cnt[kWarps][MOE_MAX_EXPERTS];
+  __shared__ int excl[MOE_MAX_EXPERTS];                    // slots of each expert in blocks 0..b-1
+  __shared__ int cnt[MOE_MAX_EXPERTS];                     // totals
+  __shared__ int tile_first[MOE_MAX_EXPERTS + 1];          // exclusive scan of the tiles per expert
+  __shared__ int part[kIdxThreads];
+  __shared__ int wsum_c[kWarps], wsum_t[kWarps];
+  __shared__ bool ready;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int b = blockIdx.x;
   const int64_t n = (int64_t)T * k;
   const int64_t base = (int64_t)b * kIdxChunk;
   const int64_t send = base + kIdxChunk < n ? base + kIdxChunk : n;   // this block's slots: [base, send)
-  // route the tokens of slots [base, send)
+  for (int i = tid; i < kWarps * MOE_MAX_EXPERTS; i += kIdxThreads) (&warp_cnt[0][0])[i] = 0;
+  // 1. route the tokens of slots [base, send), a pair of lanes per token
   const int64_t t_first = base / k, t_last = (send - 1) / k;
-  for (int64_t t = t_first + tid; t <= t_last; t += kIdxThreads) {
+  for (int64_t t0 = t_first; t0 <= t_last; t0 += kIdxThreads / 2) {   // the same trip count in every lane
+    const int64_t t = t0 + (tid >> 1);
+    const bool active = t <= t_last;
     int ti[KMAX];
     float w[KMAX];
-    route_token<KMAX>(logits, t, E, k, ti, w);
-    const bool owner = t * k >= base;
+    route_token_pair<KMAX>(logits, t, active, E, k, ti, w);
+    if (active && (tid & 1) == 0) {
+      const bool owner = t * k >= base;
 #pragma unroll
-    for (int j = 0; j < KMAX; ++j)
-      if (j < k) {
-        const int64_t s = t * k + j;
-        if (s >= base && s < send) sk[s - base] = ti[j];
-        if (owner) {
-          topk_idx[s] = ti[j];
-          topk_w[s] = w[j];
+      for (int j = 0; j < KMAX; ++j)
+        if (j < k) {
+          const int64_t s = t * k + j;
+          if (s >= base && s < send) sk[s - base] = ti[j];
+          if (owner) {
+            topk_idx[s] = ti[j];
+            topk_w[s] = w[j];
+          }
         }
-      }
+    }
   }
   __syncthreads();
+  // 2. stable ranks: a warp's running count per expert, then the earlier warps' counts
   int key[kIdxItems], rank[kIdxItems];
+  const unsigned lt_mask = (1u << lane) - 1u;
 #pragma unroll
   for (int i = 0; i < kIdxItems; ++i) {
-    const int64_t s = base + i * kIdxThreads + tid;
+    const int64_t s = base + warp * kWarpSlots + i * 32 + lane;
     key[i] = s < send ? sk[s - base] : -1;
+    const unsigned peers = __match_any_sync(0xffffffffu, key[i]);
+    const int before = key[i] >= 0 ? warp_cnt[warp][key[i]] : 0;
+    rank[i] = before + __popc(peers & lt_mask);
+    __syncwarp();
+    if (key[i] >= 0 && lane == __ffs(peers) - 1) warp_cnt[warp][key[i]] = before + __popc(peers);
+    __syncwarp();
   }
-  block_ranks(key, rank, warp_cnt, run, E);
-  for (int e = tid; e < E; e += kIdxThreads)
-    if (run[e]) atomicAdd(acc + e, run[e]);
+  __syncthreads();
+  // 3. publish: per-expert exclusive scan over the warps, the block's row of agg, the totals
+  for (int e = tid; e < E; e += kIdxThreads) {
+    int r = 0;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) {
+      const int c = warp_cnt[w][e];
+      warp_cnt[w][e] = r;
+      r += c;
+    }
+    agg[(size_t)b * E + e] = r;
+    if (r) atomicAdd(acc + e, r);
+  }
   __threadfence();
   __syncthreads();
-  if (tid == 0) is_last = atomicAdd(&hdr->tickets[0], 1u) == gridDim.x - 1;
-  __syncthreads();
-  if (is_last) {
-    __threadfence();
-    if (tid < 32) scan_counts(acc, E, BM, counts, offsets, tile_offsets);
-    __threadfence();
-    __syncthreads();
-    if (tid == 0) atomicExch(&hdr->tickets[2], 1u);   // the scans are visible
-  }
-  block_lookback(b, E, run, excl, lookback, hdr, false);
-  if (tid == 0) {   // wait for the scans, bounded
+#pragma unroll
+  for (int i = 0; i < kIdxItems; ++i)
+    if (key[i] >= 0) rank[i] += warp_cnt[warp][key[i]];
+  if (tid == 0) {   // count in, then wait (bounded) for every block to have done the same
+    atomicAdd(&hdr->tickets[0], 1u);
     bool ok = true;
     const uint64_t t0 = global_ns();
-    while (atomicAdd(&hdr->tickets[2], 0u) == 0u) {
+    while (*reinterpret_cast<volatile uint32_t *>(&hdr->tickets[0]) < gridDim.x) {
       if (global_ns() - t0 > kWaitLimitNs) {
         report(hdr, MOE_ERR_DEVICE_TIMEOUT, b);
         ok = false;
         break;
       }
-      __nanosleep(128);
+      __nanosleep(32);
     }
     __threadfence();
     ready = ok;
   }
   __syncthreads();
   if (!ready) return;
-  for (int e = tid; e < E; e += kIdxThreads) row_base[e] = __ldcg(tile_offsets + e) * BM;
+  // totals (threads 0..E-1) and this block's offset per expert: thread (e, q) sums the rows of the
+  // blocks p < b with p = q mod parts, sixteen loads in flight
+  const int parts = kIdxThreads / E;   // E <= MOE_MAX_EXPERTS == kIdxThreads
+  const int eq = tid % E, q = tid / E;
+  const int c = tid < E ? __ldcg(acc + tid) : 0;
+  int sum = 0;
+  if (q < parts) {
+    for (int p0 = q; p0 < b; p0 += 16 * parts) {
+      int v[16];
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        const int p = p0 + j * parts;
+        v[j] = p < b ? __ldcg(agg + (size_t)p * E + eq) : 0;
+      }
+#pragma unroll
+      for (int j = 0; j < 16; ++j) sum += v[j];
+    }
+  }
+  part[tid] = sum;
+  // exclusive scans of the totals and of their tile counts over the experts
+  const int tl = (c + BM - 1) / BM;
+  int ic = c, it = tl;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int a = __shfl_up_sync(0xffffffffu, ic, off), d = __shfl_up_sync(0xffffffffu, it, off);
+    if (lane >= off) {
+      ic += a;
+      it += d;
+    }
+  }
+  if (lane == 31) {
+    wsum_c[warp] = ic;
+    wsum_t[warp] = it;
+  }
   __syncthreads();
+  if (tid < E) {
+    int pc = 0, pt = 0;
+    for (int w = 0; w < warp; ++w) {
+      pc += wsum_c[w];
+      pt += wsum_t[w];
+    }
+    const int oc = pc + ic - c, ot = pt + it - tl;
+    int x = 0;
+    for (int j = 0; j < parts; ++j) x += part[j * E + tid];
+    excl[tid] = x;
+    cnt[tid] = c;
+    tile_first[tid] = ot;
+    if (tid == E - 1) tile_first[E] = ot + tl;
+    if (b == 0) {
+      counts[tid] = c;
+      offsets[tid] = oc;
+      tile_offsets[tid] = ot;
+      if (tid == E - 1) {
+        offsets[E] = oc + c;
+        tile_offsets[E] = ot + tl;
+      }
+    }
+  }
+  __syncthreads();
+  // 4. scatter
 #pragma unroll
   for (int i = 0; i < kIdxItems; ++i) {
-    const int64_t s = base + i * kIdxThreads + tid;
-    if (s >= send) continue;
-    const int row = row_base[key[i]] + excl[key[i]] + rank[i];
+    const int64_t s = base + warp * kWarpSlots + i * 32 + lane;
+    if (s >= send || key[i] < 0) continue;
+    const int row = tile_first[key[i]] * BM + excl[key[i]] + rank[i];
     row_of_slot[s] = row;
     token_of_row[row] = (int)(s / k);
   }
-  for (int e = blockIdx.x; e < E; e += gridDim.x) {   // padding rows of the grouped layout
-    const int start = __ldcg(tile_offsets + e) * BM + __ldcg(counts + e), end = __ldcg(tile_offsets + e + 1) * BM;
+  for (int e = b; e < E; e += gridDim.x) {   // padding rows of the grouped layout
+    const int start = tile_first[e] * BM + cnt[e], end = tile_first[e + 1] * BM;
     for (int r = start + tid; r < end; r += kIdxThreads) token_of_row[r] = -1;
   }
 }
@@ -484,7 +620,7 @@ static int launch_route_count_index(const float *logits, int T, int E, int k, in
                                     int32_t *token_of_row, void *ws, cudaStream_t s, bool *launched) {
   *launched = false;
   const int nb = (int)index_blocks(T, k);
-  int per_sm = 0;   // every block must be resident at once (the blocks wait for the last one's scans)
+  int per_sm = 0;   // every block must be resident at once (each waits until all have published)
   if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, route_count_index_kernel<KMAX>, kIdxThreads, 0) !=
       cudaSuccess) {
     (void)cudaGetLastError();
@@ -494,10 +630,11 @@ static int launch_route_count_index(const float *logits, int T, int E, int k, in
   char *w = static_cast<char *>(ws);
   IndexWs *iw = reinterpret_cast<IndexWs *>(w);
   int32_t *acc = reinterpret_cast<int32_t *>(w + sizeof(IndexWs));
-  uint64_t *lookback = reinterpret_cast<uint64_t *>(w + sizeof(IndexWs) + acc_bytes(E) + kHookBytes);
-  // status, tickets, totals and every look-back word start at zero (the fault hook is cleared too)
-  MOE_TRY_CUDA(cudaMemsetAsync(w, 0, sizeof(IndexWs) + acc_bytes(E) + kHookBytes + (size_t)nb * E * sizeof(uint64_t),
-                               s));
+  // the blocks' per-expert counts, [nb][E] int32, in the look-back words' space (every block writes
+  // its whole row before any block reads it, so the rows need no reset)
+  int32_t *agg = reinterpret_cast<int32_t *>(w + sizeof(IndexWs) + acc_bytes(E) + kHookBytes);
+  // status, tickets and totals start at zero (the fault hook is cleared too)
+  MOE_TRY_CUDA(cudaMemsetAsync(w, 0, sizeof(IndexWs) + acc_bytes(E) + kHookBytes, s));
   // A cooperative launch: CUDA starts the grid only when all of its blocks can be resident together,
   // also while kernels from other streams (another layer, even another fused call) hold SMs, so the
   // blocks' meeting point cannot wait on a block that is still queued.
@@ -511,7 +648,7 @@ static int launch_route_count_index(const float *logits, int T, int E, int k, in
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   const cudaError_t e = cudaLaunchKernelEx(&cfg, route_count_index_kernel<KMAX>, logits, T, E, k, (int)MOE_GROUP_ROWS,
-                                           &iw->hdr, acc, lookback, topk_idx, topk_w, counts, offsets, tile_offsets,
+                                           &iw->hdr, acc, agg, topk_idx, topk_w, counts, offsets, tile_offsets,
                                            row_of_slot, token_of_row);
   if (e == cudaErrorCooperativeLaunchTooLarge) {   // the grid cannot be resident at once: two launches
     (void)cudaGetLastError();
