@@ -24,6 +24,10 @@ constexpr int kRouteThreads = 128;               // tokens (threads) per routing
 constexpr int kIdxThreads = 256;                 // 8 warps
 constexpr int kIdxItems = 4;                     // slots per thread
 constexpr int kIdxChunk = kIdxThreads * kIdxItems;
+// The fused routing kernel's blocks own kIdxThreads * ITEMS slots, ITEMS = 2 (twice the index
+// kernel's blocks, so twice the SMs route) while that is at most one block per SM, else 4. Its
+// per-block count table ([blocks][E] int32) lives in the index kernel's look-back words
+// ([blocks][E] uint64 at kIdxChunk slots per block), which it fits for ITEMS >= kIdxItems / 2.
 
 // look-back word: flag in the high 32 bits, value in the low 32 bits
 constexpr uint64_t kFlagAggregate = 1ull << 32;
@@ -308,12 +312,12 @@ __global__ void __launch_bounds__(kIdxThreads) index_kernel(const int32_t *__res
 
 // ---------------------------------------------------------------------------------------------
 // Routing, counting and index generation in one kernel (moe_route_count_index). Block b owns the
-// same kIdxChunk slots as index_kernel's block b.
+// C = kIdxThreads * ITEMS slots [b C, (b + 1) C).
 //   1. Routing: each token of the block's slots is routed by a pair of adjacent lanes, each lane
 //      keeping the top-k of one half of the experts; the lower lane merges the upper lane's list
 //      into its own (route_token_pair). A token whose slots straddle two blocks is routed by both,
 //      identically; the block holding its first slot writes topk_idx / topk_w.
-//   2. Ranks: warp w owns slots [w*128, w*128+128) of the chunk, four rounds of 32; a slot's rank
+//   2. Ranks: warp w owns slots [32 ITEMS w, 32 ITEMS (w + 1)) of the chunk, ITEMS rounds of 32; a slot's rank
 //      within its expert is the warp's running count (match.any per round, no block barrier),
 //      plus the slots of that expert in the block's earlier warps.
 //   3. The block publishes its per-expert counts (one row of agg) and adds them to the totals acc,
@@ -377,26 +381,27 @@ __device__ __forceinline__ void route_token_pair(const float *__restrict__ logit
   for (int j = 0; j < KMAX; ++j) w[j] = w[j] / s;
 }
 
-template <int KMAX>
+template <int KMAX, int ITEMS>
 __global__ void __launch_bounds__(kIdxThreads) route_count_index_kernel(
     const float *__restrict__ logits, int T, int E, int k, int BM, WsHeader *hdr, int32_t *acc,
     int32_t *agg, int32_t *__restrict__ topk_idx, float *__restrict__ topk_w, int32_t *__restrict__ counts,
     int32_t *__restrict__ offsets, int32_t *__restrict__ tile_offsets, int32_t *__restrict__ row_of_slot,
     int32_t *__restrict__ token_of_row) {
-  constexpr int kWarps = kIdxThreads / 32, kWarpSlots = 32 * kIdxItems;
-  __shared__ int sk[kIdxChunk];                            // experts of this block's slots, slot order
+  static_assert(2 * ITEMS >= kIdxItems, "the count table must fit the look-back words");
+  constexpr int kWarps = kIdxThreads / 32, kWarpSlots = 32 * ITEMS, kRciChunk = kIdxThreads * ITEMS;
+  __shared__ int sk[kRciChunk];                            // experts of this block's slots, slot order
   __shared__ int warp_cnt[kWarps][MOE_MAX_EXPERTS];
   __shared__ int excl[MOE_MAX_EXPERTS];                    // slots of each expert in blocks 0..b-1
   __shared__ int cnt[MOE_MAX_EXPERTS];                     // totals
   __shared__ int tile_first[MOE_MAX_EXPERTS + 1];          // exclusive scan of the tiles per expert
-  __shared__ int part[kIdxThreads];
+  __shared__ __align__(16) int part[4 * kIdxThreads];
   __shared__ int wsum_c[kWarps], wsum_t[kWarps];
   __shared__ bool ready;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int b = blockIdx.x;
   const int64_t n = (int64_t)T * k;
-  const int64_t base = (int64_t)b * kIdxChunk;
-  const int64_t send = base + kIdxChunk < n ? base + kIdxChunk : n;   // this block's slots: [base, send)
+  const int64_t base = (int64_t)b * kRciChunk;
+  const int64_t send = base + kRciChunk < n ? base + kRciChunk : n;   // this block's slots: [base, send)
   for (int i = tid; i < kWarps * MOE_MAX_EXPERTS; i += kIdxThreads) (&warp_cnt[0][0])[i] = 0;
   // 1. route the tokens of slots [base, send), a pair of lanes per token
   const int64_t t_first = base / k, t_last = (send - 1) / k;
@@ -422,10 +427,10 @@ __global__ void __launch_bounds__(kIdxThreads) route_count_index_kernel(
   }
   __syncthreads();
   // 2. stable ranks: a warp's running count per expert, then the earlier warps' counts
-  int key[kIdxItems], rank[kIdxItems];
+  int key[ITEMS], rank[ITEMS];
   const unsigned lt_mask = (1u << lane) - 1u;
 #pragma unroll
-  for (int i = 0; i < kIdxItems; ++i) {
+  for (int i = 0; i < ITEMS; ++i) {
     const int64_t s = base + warp * kWarpSlots + i * 32 + lane;
     key[i] = s < send ? sk[s - base] : -1;
     const unsigned peers = __match_any_sync(0xffffffffu, key[i]);
@@ -451,7 +456,7 @@ __global__ void __launch_bounds__(kIdxThreads) route_count_index_kernel(
   __threadfence();
   __syncthreads();
 #pragma unroll
-  for (int i = 0; i < kIdxItems; ++i)
+  for (int i = 0; i < ITEMS; ++i)
     if (key[i] >= 0) rank[i] += warp_cnt[warp][key[i]];
   if (tid == 0) {   // count in, then wait (bounded) for every block to have done the same
     atomicAdd(&hdr->tickets[0], 1u);
@@ -470,25 +475,49 @@ __global__ void __launch_bounds__(kIdxThreads) route_count_index_kernel(
   }
   __syncthreads();
   if (!ready) return;
-  // totals (threads 0..E-1) and this block's offset per expert: thread (e, q) sums the rows of the
-  // blocks p < b with p = q mod parts, sixteen loads in flight
-  const int parts = kIdxThreads / E;   // E <= MOE_MAX_EXPERTS == kIdxThreads
-  const int eq = tid % E, q = tid / E;
+  // totals (threads 0..E-1) and this block's offset per expert: a row of the count table is read by
+  // Q threads (16-byte loads of four experts when E % 4 == 0, else one expert each); thread
+  // (eq, q) sums the rows of the blocks p < b with p = q mod parts, eight loads in flight, into
+  // part[q * E + expert]
+  const bool vec4 = (E & 3) == 0;   // rows then start on 16-byte boundaries
+  const int Q = vec4 ? E / 4 : E;
+  const int parts = kIdxThreads / Q;   // E <= MOE_MAX_EXPERTS == kIdxThreads
+  const int eq = tid % Q, q = tid / Q;
   const int c = tid < E ? __ldcg(acc + tid) : 0;
-  int sum = 0;
   if (q < parts) {
-    for (int p0 = q; p0 < b; p0 += 16 * parts) {
-      int v[16];
+    if (vec4) {
+      int4 sum = make_int4(0, 0, 0, 0);
+      for (int p0 = q; p0 < b; p0 += 8 * parts) {
+        int4 v[8];
 #pragma unroll
-      for (int j = 0; j < 16; ++j) {
-        const int p = p0 + j * parts;
-        v[j] = p < b ? __ldcg(agg + (size_t)p * E + eq) : 0;
+        for (int j = 0; j < 8; ++j) {
+          const int p = p0 + j * parts;
+          v[j] = p < b ? __ldcg(reinterpret_cast<const int4 *>(agg + (size_t)p * E) + eq) : make_int4(0, 0, 0, 0);
+        }
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          sum.x += v[j].x;
+          sum.y += v[j].y;
+          sum.z += v[j].z;
+          sum.w += v[j].w;
+        }
       }
+      reinterpret_cast<int4 *>(part)[tid] = sum;   // part[q * E + 4 eq + 0..3]
+    } else {
+      int sum = 0;
+      for (int p0 = q; p0 < b; p0 += 8 * parts) {
+        int v[8];
 #pragma unroll
-      for (int j = 0; j < 16; ++j) sum += v[j];
+        for (int j = 0; j < 8; ++j) {
+          const int p = p0 + j * parts;
+          v[j] = p < b ? __ldcg(agg + (size_t)p * E + eq) : 0;
+        }
+#pragma unroll
+        for (int j = 0; j < 8; ++j) sum += v[j];
+      }
+      part[tid] = sum;   // part[q * E + eq]
     }
   }
-  part[tid] = sum;
   // exclusive scans of the totals and of their tile counts over the experts
   const int tl = (c + BM - 1) / BM;
   int ic = c, it = tl;
@@ -531,12 +560,12 @@ __global__ void __launch_bounds__(kIdxThreads) route_count_index_kernel(
   __syncthreads();
   // 4. scatter
 #pragma unroll
-  for (int i = 0; i < kIdxItems; ++i) {
+  for (int i = 0; i < ITEMS; ++i) {
     const int64_t s = base + warp * kWarpSlots + i * 32 + lane;
     if (s >= send || key[i] < 0) continue;
     const int row = tile_first[key[i]] * BM + excl[key[i]] + rank[i];
     row_of_slot[s] = row;
-    token_of_row[row] = (int)(s / k);
+    token_of_row[row] = (int)s / k;   // s < T*k < 2^31
   }
   for (int e = b; e < E; e += gridDim.x) {   // padding rows of the grouped layout
     const int start = tile_first[e] * BM + cnt[e], end = tile_first[e + 1] * BM;
@@ -614,15 +643,18 @@ extern "C" int moe_count_index(const int32_t *topk_idx, int T, int k, int E, int
   return MOE_OK;
 }
 
-template <int KMAX>
-static int launch_route_count_index(const float *logits, int T, int E, int k, int32_t *topk_idx, float *topk_w,
-                                    int32_t *counts, int32_t *offsets, int32_t *tile_offsets, int32_t *row_of_slot,
-                                    int32_t *token_of_row, void *ws, cudaStream_t s, bool *launched) {
+// Launch route_count_index_kernel<KMAX, ITEMS> if its whole grid fits on the GPU at once; *launched
+// tells whether it did (if not, nothing was enqueued).
+template <int KMAX, int ITEMS>
+static int launch_rci(const float *logits, int T, int E, int k, int32_t *topk_idx, float *topk_w, int32_t *counts,
+                      int32_t *offsets, int32_t *tile_offsets, int32_t *row_of_slot, int32_t *token_of_row, void *ws,
+                      cudaStream_t s, bool *launched) {
   *launched = false;
-  const int nb = (int)index_blocks(T, k);
+  const int64_t chunk = (int64_t)kIdxThreads * ITEMS;
+  const int64_t nb = ((int64_t)T * k + chunk - 1) / chunk;
   int per_sm = 0;   // every block must be resident at once (each waits until all have published)
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, route_count_index_kernel<KMAX>, kIdxThreads, 0) !=
-      cudaSuccess) {
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, route_count_index_kernel<KMAX, ITEMS>, kIdxThreads,
+                                                    0) != cudaSuccess) {
     (void)cudaGetLastError();
     return MOE_OK;
   }
@@ -647,16 +679,30 @@ static int launch_route_count_index(const float *logits, int T, int E, int k, in
   attr[0].val.cooperative = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  const cudaError_t e = cudaLaunchKernelEx(&cfg, route_count_index_kernel<KMAX>, logits, T, E, k, (int)MOE_GROUP_ROWS,
-                                           &iw->hdr, acc, agg, topk_idx, topk_w, counts, offsets, tile_offsets,
-                                           row_of_slot, token_of_row);
-  if (e == cudaErrorCooperativeLaunchTooLarge) {   // the grid cannot be resident at once: two launches
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, route_count_index_kernel<KMAX, ITEMS>, logits, T, E, k,
+                                           (int)MOE_GROUP_ROWS, &iw->hdr, acc, agg, topk_idx, topk_w, counts,
+                                           offsets, tile_offsets, row_of_slot, token_of_row);
+  if (e == cudaErrorCooperativeLaunchTooLarge) {   // the grid cannot be resident at once
     (void)cudaGetLastError();
     return MOE_OK;
   }
   MOE_TRY_CUDA(e);
   *launched = true;
   return MOE_OK;
+}
+
+// 512 slots per block while that is at most one block per SM (more blocks than SMs route no faster
+// and lengthen every block's sum over its predecessors' counts), else 1024.
+template <int KMAX>
+static int launch_route_count_index(const float *logits, int T, int E, int k, int32_t *topk_idx, float *topk_w,
+                                    int32_t *counts, int32_t *offsets, int32_t *tile_offsets, int32_t *row_of_slot,
+                                    int32_t *token_of_row, void *ws, cudaStream_t s, bool *launched) {
+  const int64_t nb512 = ((int64_t)T * k + 2 * kIdxThreads - 1) / (2 * kIdxThreads);
+  if (nb512 <= sm_count())
+    return launch_rci<KMAX, 2>(logits, T, E, k, topk_idx, topk_w, counts, offsets, tile_offsets, row_of_slot,
+                               token_of_row, ws, s, launched);
+  return launch_rci<KMAX, 4>(logits, T, E, k, topk_idx, topk_w, counts, offsets, tile_offsets, row_of_slot,
+                             token_of_row, ws, s, launched);
 }
 
 extern "C" int moe_route_count_index(const float *logits, int T, int E, int k, int32_t *topk_idx, float *topk_w,

@@ -1,8 +1,10 @@
 """moe_route_count_index (routing, counting and index generation in one launch) must give, bit for
 bit, what moe_route_topk followed by moe_count_index gives: the same kernels' selection and
 weights, and the same stable counting sort. Shapes cover tokens whose slots straddle two blocks
-(k = 3, 5), E = 256 with k = 16, a problem near the limit of blocks that fit at once, one above it
-(the call then makes the two calls itself), exact ties, and calls back to back on one workspace."""
+(k = 3, 5), E = 256 with k = 16, the largest problems of the kernel's two block sizes (512 slots
+while that is at most one block per SM, then 1024 while every block fits on the GPU at once), one
+above both (the call then makes the two calls itself), exact ties, and calls back to back on one
+workspace."""
 import pytest
 import torch
 
@@ -12,8 +14,9 @@ pytestmark = pytest.mark.gpu
 
 SHAPES = [(1, 8, 2, "normal"), (5, 256, 16, "normal"), (1023, 7, 3, "normal"), (1025, 1, 1, "normal"),
           (333, 40, 5, "zipf"), (8192, 64, 8, "router"), (16384, 64, 8, "uniform"), (16384, 128, 8, "zipf"),
-          (100000, 64, 3, "normal"),      # 300,000 slots: near the fused kernel's limit
-          (40000, 256, 16, "zipf"),       # 640,000 slots: above it, the call falls back to two launches
+          (25000, 64, 3, "normal"),       # 75,000 slots: 147 blocks of 512 slots
+          (100000, 64, 3, "normal"),      # 300,000 slots: 293 blocks of 1024 slots (2 per SM)
+          (40000, 256, 16, "zipf"),       # 640,000 slots: above both, the call falls back to two launches
           (777, 16, 4, "ties")]
 
 
