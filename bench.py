@@ -44,7 +44,7 @@ METRIC_FWD = "MoE layer fwd tokens/s (E=64,k=8,d=2048); grouped-GEMM % BF16 peak
 # kernel changes, its traffic is unmeasured (null) until it is captured again.
 GEMM_SOURCES = ("gemm_rows.cu", "gemm_tc.cu", "tc_ptx.cuh", "tma_host.cuh", "common.cuh")
 GEMM_TRAFFIC = {    # workload -> (bytes per step, source digest)
-    "fwdbwd_t8192": (5756257536, "1c6523dd79350411"),
+    "fwdbwd_t8192": (5756363008, "1a2a8dd03b616ac3"),
 }
 DEFAULT_WORKLOAD = "fwdbwd_t8192"
 
@@ -221,11 +221,12 @@ def run_ours(args):
         if not args.gather:
             L.moe_permute(x, w.k, w.E, layer.row_of_slot, layer.counts, layer.tile_offsets, layer.x_perm)
         ev[3].record(stream)
+        ab = layer.ab if bwd and not args.recompute else None   # as MoELayer.forward: stored only for a backward
         if args.gather:
-            L.moe_grouped_ffn_fwd_gather(x, layer.token_of_row, wgu, wd, layer.tile_offsets, layer.offsets, layer.ab,
+            L.moe_grouped_ffn_fwd_gather(x, layer.token_of_row, wgu, wd, layer.tile_offsets, layer.offsets, ab,
                                          layer.h, layer.y_perm, layer.ws_ffn)
         else:
-            L.moe_grouped_ffn_fwd(layer.x_perm, wgu, wd, layer.tile_offsets, layer.offsets, layer.ab, layer.h,
+            L.moe_grouped_ffn_fwd(layer.x_perm, wgu, wd, layer.tile_offsets, layer.offsets, ab, layer.h,
                                   layer.y_perm, layer.ws_ffn)
         ev[4].record(stream)
         L.moe_combine_fwd(layer.y_perm, layer.topk_w, layer.row_of_slot, w.T, w.k, layer.out)

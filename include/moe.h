@@ -177,7 +177,10 @@ int moe_permute(const void *x, int dtype, int T, int d, int k, int E, const int3
  *   x_perm    [rows_max, d]   grouped tokens
  *   w_gate_up [E, 2f, d]      rows 0..f-1: gate projection Wg[e]; rows f..2f-1: up projection Wu[e]
  *   w_down    [E, d, f]       Wd[e]
- *   ab        [rows_max, 2f]  saved for backward: columns 0..f-1 a = x Wg^T, f..2f-1 b = x Wu^T
+ *   ab        [rows_max, 2f]  saved for backward: columns 0..f-1 a = x Wg^T, f..2f-1 b = x Wu^T;
+ *                             may be NULL, and a, b are then not stored: a forward that no
+ *                             moe_grouped_ffn_bwd on these activations follows (inference, or a
+ *                             layer whose backward recomputes them, moe_grouped_ffn_bwd_recompute)
  *   h         [rows_max, f]   saved: silu(a) * b
  *   y_perm    [rows_max, d]   h Wd^T
  * GEMM1 fuses the SwiGLU gate into its epilogue; GEMM2 is a plain grouped GEMM. bf16: tcgen05

@@ -192,7 +192,7 @@ def moe_grouped_ffn_fwd_gather(x, token_of_row, w_gate_up, w_down, tile_offsets,
     E, twof, d = w_gate_up.shape
     _ok("moe_grouped_ffn_fwd_gather", lib().moe_grouped_ffn_fwd_gather(
         _p(x), _p(token_of_row), x.shape[0], _p(w_gate_up), _p(w_down), _p(tile_offsets), _p(offsets), E, d,
-        twof // 2, ab.shape[0], dtype_code(x.dtype), _p(ab), _p(h), _p(y_perm), _p(ws), ws.numel() * ws.element_size(),
+        twof // 2, h.shape[0], dtype_code(x.dtype), _p(ab), _p(h), _p(y_perm), _p(ws), ws.numel() * ws.element_size(),
         _s(stream)))
 
 

@@ -51,9 +51,10 @@ static int ffn_fwd(const void *x, const int32_t *tor, int T, bool gather, const 
   if (rc) return rc;
   if (rows_max == 0) return MOE_OK;
   if ((rc = check_tokens(x, tor, gather, T))) return rc;
-  const void *ptrs[] = {w_gate_up, w_down, ab, h, y_perm};
+  const void *ptrs[] = {w_gate_up, w_down, h, y_perm};
   for (const void *q : ptrs)
     if (!q || !aligned16(q)) return MOE_ERR_INVALID_ARG;
+  if (ab && !aligned16(ab)) return MOE_ERR_INVALID_ARG;   // null: a, b are not stored
   if (!tile_offsets || !offsets) return MOE_ERR_INVALID_ARG;
   cudaStream_t s = (cudaStream_t)stream;
   if (dtype == MOE_F32)

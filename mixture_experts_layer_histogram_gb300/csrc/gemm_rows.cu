@@ -99,7 +99,7 @@ struct Params {
   int a_rows_e;                  // rows of the weight's 2D view per expert (DOWN, DH, DGRAD)
   int f;                         // GATEUP, DH: column of b in ab / dab
   int64_t rows_max;              // rows of every grouped buffer (bounds the zero-padding writes)
-  __nv_bfloat16 *out0;           // zero padding rows: GATEUP ab, DOWN y, DH dab, DGRAD dx
+  __nv_bfloat16 *out0;           // zero padding rows: GATEUP ab (null: a, b not stored), DOWN y, DH dab, DGRAD dx
   int64_t ld0;
   __nv_bfloat16 *out1;           // GATEUP h
   int64_t ld1;
@@ -506,10 +506,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(G ? THREADS_G : THRE
               ph[s][c] = pack_bf16x2(a0 * sigmoidf_(a0) * b0, a1 * sigmoidf_(a1) * b1);
             }
           }
-          // three [32 tokens][16 features] blocks (32-byte rows, 32-byte swizzle)
+          // three [32 tokens][16 features] blocks (32-byte rows, 32-byte swizzle); a and b only when
+          // they are stored
           const uint32_t(*blk[3])[4] = {pa, pb, ph};
 #pragma unroll
           for (int o = 0; o < 3; ++o) {
+            if (o < 2 && p.out0 == nullptr) continue;
             const uint32_t buf = wbuf + (uint32_t)bi * C::BUF_BYTES;
             if (lane == 0) asm volatile("cp.async.bulk.wait_group.read 3;" ::: "memory");   // buf's last store read it
             __syncwarp();
@@ -615,8 +617,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(G ? THREADS_G : THRE
       const int zend = (int64_t)t.zero_end < p.rows_max ? t.zero_end : (int)p.rows_max;
       for (int y = t.start + t.nt + 32 * hh; y + 32 <= zend; y += 64) {
         if (K == GATEUP) {
-          zero_rows(p.out0, p.ld0, y, fcol, 16, lane);
-          zero_rows(p.out0, p.ld0, y, p.f + fcol, 16, lane);
+          if (p.out0) {
+            zero_rows(p.out0, p.ld0, y, fcol, 16, lane);
+            zero_rows(p.out0, p.ld0, y, p.f + fcol, 16, lane);
+          }
           zero_rows(p.out1, p.ld1, y, fcol, 16, lane);
         } else if (K == DH) {
           zero_rows(p.out0, p.ld0, y, fcol, 32, lane);
@@ -674,9 +678,10 @@ int rows_gateup(const void *x_perm, const void *wgu, const int32_t *tile_offsets
                 int f, int64_t rows_max, void *ab, void *h, WsHeader *hdr, cudaStream_t s) {
   using namespace tc;
   using namespace tc::rows;
-  CUtensorMap mA, mB, mC0, mC1;
+  CUtensorMap mA, mB, mC0, mC1;   // ab == nullptr: a, b are not stored (mC0 is then a stand-in, unused)
   if (!make_gateup_map(&mA, wgu, E, f, d) || !make_map(&mB, x_perm, rows_max, d, TOK_ROWS) ||
-      !make_store_map16(&mC0, ab, rows_max, 2 * f) || !make_store_map16(&mC1, h, rows_max, f))
+      !(ab ? make_store_map16(&mC0, ab, rows_max, 2 * f) : make_store_map16(&mC0, h, rows_max, f)) ||
+      !make_store_map16(&mC1, h, rows_max, f))
     return MOE_ERR_CUDA;
   rows::Params p{};
   p.tile_offsets = tile_offsets;
@@ -701,8 +706,9 @@ int rows_gateup_gather(const void *x, const int32_t *token_of_row, int T, const 
                        cudaStream_t s) {
   using namespace tc;
   using namespace tc::rows;
-  CUtensorMap mA, mC0, mC1;
-  if (!make_gateup_map(&mA, wgu, E, f, d) || !make_store_map16(&mC0, ab, rows_max, 2 * f) ||
+  CUtensorMap mA, mC0, mC1;   // ab == nullptr: a, b are not stored (mC0 is then a stand-in, unused)
+  if (!make_gateup_map(&mA, wgu, E, f, d) ||
+      !(ab ? make_store_map16(&mC0, ab, rows_max, 2 * f) : make_store_map16(&mC0, h, rows_max, f)) ||
       !make_store_map16(&mC1, h, rows_max, f))
     return MOE_ERR_CUDA;
   rows::Params p{};

@@ -103,8 +103,10 @@ __global__ void __launch_bounds__(256) simt_gemm_kernel(const Args p) {
     if (m >= M) continue;
     if (KIND == GATEUP) {
       const float a = acc[i], b = acc2[i];
-      p.C[m * p.ldc + n] = a;
-      p.C[m * p.ldc + p.f + n] = b;
+      if (p.C) {   // null: a, b are not stored
+        p.C[m * p.ldc + n] = a;
+        p.C[m * p.ldc + p.f + n] = b;
+      }
       p.C2[m * p.ldc2 + n] = a / (1.0f + expf(-a)) * b;
     } else if (KIND == DH) {
       const float dh = acc[i], a = p.aux[m * p.ld_aux + n], b = p.aux[m * p.ld_aux + p.f + n];

@@ -101,13 +101,16 @@ class MoELayer:
             L.moe_route_count_index(logits, self.k, self.topk_idx, self.topk_w, self.counts, self.offsets,
                                     self.tile_offsets, self.row_of_slot, self.token_of_row, self.ws_index, stream)
             self._x = self._w_router = None
+        # a and b are stored only for a backward that reads them (not for a forward-only layer, nor for
+        # the recomputing backward, which forms them again)
+        ab = self.ab if self.backward_enabled and not self.recompute else None
         if self.gather:
             self._xin = x
             L.moe_grouped_ffn_fwd_gather(x, self.token_of_row, w_gate_up, w_down, self.tile_offsets, self.offsets,
-                                         self.ab, self.h, self.y_perm, self.ws_ffn, stream)
+                                         ab, self.h, self.y_perm, self.ws_ffn, stream)
         else:
             L.moe_permute(x, self.k, self.E, self.row_of_slot, self.counts, self.tile_offsets, self.x_perm, stream)
-            L.moe_grouped_ffn_fwd(self.x_perm, w_gate_up, w_down, self.tile_offsets, self.offsets, self.ab, self.h,
+            L.moe_grouped_ffn_fwd(self.x_perm, w_gate_up, w_down, self.tile_offsets, self.offsets, ab, self.h,
                                   self.y_perm, self.ws_ffn, stream)
         L.moe_combine_fwd(self.y_perm, self.topk_w, self.row_of_slot, self.T, self.k, self.out, stream)
         return self.out

@@ -4,7 +4,10 @@ gate/up weight gradient read token rows of x through token_of_row instead of row
 The same bytes reach the tensor cores either way, so every output of a layer pass in gather mode
 must equal, bit for bit, the output of the pass that runs moe_permute first; the gather path is also
 compared with the fp64 oracle directly, on small shapes element by element and at the benchmark size
-on sampled tokens."""
+on sampled tokens.
+
+A forward-only layer (and the recomputing one) passes no ab buffer: GEMM1 then stores h but not a and
+b. Its output must equal the training layer's, bit for bit, and the ab buffer must stay untouched."""
 import numpy as np
 import pytest
 import torch
@@ -46,6 +49,21 @@ def test_gather_pass_is_bit_identical_to_permute_pass(w):
     assert torch.equal(out0, out1)
     for k in KEYS:
         assert torch.equal(r0[k], r1[k]), k
+
+
+@pytest.mark.parametrize("gather", [False, True])
+@pytest.mark.parametrize("w", CASES, ids=lambda w: w.name)
+def test_forward_only_layer_stores_no_ab(w, gather):
+    from mixture_experts_layer_histogram_gb300 import MoELayer
+    inp = moe_inputs.make_all(w, "cuda")
+    _, out0, _ = _pass(w, inp, gather=False)
+    layer = MoELayer(w.T, w.d, w.E, w.k, w.f, w.torch_dtype, "cuda", backward=False, gather=gather)
+    layer.ab.fill_(float("nan"))
+    layer.forward(inp["x"], inp["logits"], inp["w_gate_up"], inp["w_down"])
+    torch.cuda.synchronize()
+    assert layer.status() == (0, 0)
+    assert torch.equal(layer.out, out0)
+    assert torch.isnan(layer.ab).all()
 
 
 @pytest.mark.parametrize("w", CASES[:2] + CASES[-1:], ids=lambda w: w.name)
