@@ -399,6 +399,9 @@ def run_ours(args):
                    "pass": (("fwd+bwd (recompute)" if args.recompute else "fwd+bwd") if bwd else "fwd") +
                            (", router GEMM in the pass" if args.router else "") +
                            (", permutation fused into the GEMM loads" if args.gather else ""),
+                   "saved_activations": ("ab and h" if bwd and not args.recompute else
+                                         "h only (no backward reads a, b)" if not bwd else
+                                         "h only (the backward recomputes a, b)"),
                    "parallelism": f"replicas x{world}", "launch": "cuda graph" if args.graph else "eager",
                    "l2": "inputs larger than L2 (expert weights 768 MiB, grouped activations > 129 MB); no flush"},
         "roofline": roofline,
