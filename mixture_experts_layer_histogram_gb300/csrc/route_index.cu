@@ -317,9 +317,9 @@ __global__ void __launch_bounds__(kIdxThreads) index_kernel(const int32_t *__res
 //      keeping the top-k of one half of the experts; the lower lane merges the upper lane's list
 //      into its own (route_token_pair). A token whose slots straddle two blocks is routed by both,
 //      identically; the block holding its first slot writes topk_idx / topk_w.
-//   2. Ranks: warp w owns slots [32 ITEMS w, 32 ITEMS (w + 1)) of the chunk, ITEMS rounds of 32; a slot's rank
-//      within its expert is the warp's running count (match.any per round, no block barrier),
-//      plus the slots of that expert in the block's earlier warps.
+//   2. Ranks: warp w owns slots [32 ITEMS w, 32 ITEMS (w + 1)) of the chunk, ITEMS rounds of 32;
+//      a slot's rank within its expert is the warp's running count (match.any per round, no block
+//      barrier), plus the slots of that expert in the block's earlier warps.
 //   3. The block publishes its per-expert counts (one row of agg) and adds them to the totals acc,
 //      then counts itself in. Once all blocks have (a bounded wait of about 0.2 s), every block
 //      reads the totals and its predecessors' rows from L2, scans the totals itself, and scatters
