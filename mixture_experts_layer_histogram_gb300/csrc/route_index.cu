@@ -66,8 +66,10 @@ __device__ __forceinline__ void route_token(const float *__restrict__ logits, in
       for (int i = 0; i < 64; ++i) v[i] = e0 + i < E ? __ldg(row + e0 + i) : 0.0f;
     }
 #pragma unroll
-    for (int i = 0; i < 64; ++i)
-      if (e0 + i < E) topk_insert<KMAX>(tv, ti, v[i], e0 + i);
+    for (int i = 0; i < 64; ++i) {   // leave at the row's end: predicated-off insertions still issue
+      if (e0 + i >= E) break;
+      topk_insert<KMAX>(tv, ti, v[i], e0 + i);
+    }
   }
   const float m = tv[0];
   float s = 0.0f;
@@ -358,8 +360,10 @@ __device__ __forceinline__ void route_token_pair(const float *__restrict__ logit
         for (int i = 0; i < 64; ++i) v[i] = e0 + i < hi ? __ldg(row + e0 + i) : 0.0f;
       }
 #pragma unroll
-      for (int i = 0; i < 64; ++i)
-        if (e0 + i < hi) topk_insert<KMAX>(tv, ti, v[i], e0 + i);
+      for (int i = 0; i < 64; ++i) {   // leave at the half's end: predicated-off insertions still issue
+        if (e0 + i >= hi) break;
+        topk_insert<KMAX>(tv, ti, v[i], e0 + i);
+      }
     }
   }
   // The upper lane's entries all carry higher ids than the lower lane's and arrive in their list
