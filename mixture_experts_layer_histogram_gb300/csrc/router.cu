@@ -103,8 +103,10 @@ __device__ __forceinline__ void take_chunk(const float (&v)[32], int c0, int E, 
     }
   }
 #pragma unroll
-  for (int i = 0; i < 32; ++i)
-    if (c0 + i < E) topk_insert<KMAX>(tv, ti, v[i], c0 + i);
+  for (int i = 0; i < 32; ++i) {   // leave at the row's end: predicated-off insertions still issue
+    if (c0 + i >= E) break;
+    topk_insert<KMAX>(tv, ti, v[i], c0 + i);
+  }
 }
 
 template <int KMAX>
