@@ -29,7 +29,9 @@ constexpr int kIdxChunk = kIdxThreads * kIdxItems;
 // per-block count table ([blocks][E] int32) lives in the index kernel's look-back words
 // ([blocks][E] uint64 at kIdxChunk slots per block), which it fits for ITEMS >= kIdxItems / 2.
 
-// look-back word: flag in the high 32 bits, value in the low 32 bits
+// look-back word: flag in the high 32 bits, value in the low 32 bits; a look-back reads this many
+// predecessors' words per round
+constexpr int kLookWindow = 8;
 constexpr uint64_t kFlagAggregate = 1ull << 32;
 constexpr uint64_t kFlagPrefix = 2ull << 32;
 
@@ -224,10 +226,10 @@ __device__ __forceinline__ void block_ranks(const int (&key)[kIdxItems], int (&r
 }
 
 // Decoupled look-back: publish block b's per-expert aggregate run[e], walk back over the preceding
-// blocks' words (an aggregate adds and continues, an inclusive prefix adds and stops, a word not
-// yet published is waited for, at most about 0.2 s), set excl[e] to the number of slots of expert
-// e in blocks 0..b-1 and publish block b's inclusive prefix. `withhold` leaves this block's words
-// unpublished (the fault hook of moe_count_index).
+// blocks' words, kLookWindow per round (an aggregate adds and continues, an inclusive prefix adds
+// and stops, a word not yet published is waited for, at most about 0.2 s in all), set excl[e] to
+// the number of slots of expert e in blocks 0..b-1 and publish block b's inclusive prefix.
+// `withhold` leaves this block's words unpublished (the fault hook of moe_count_index).
 __device__ __forceinline__ void block_lookback(int b, int E, const int *run, int *excl, uint64_t *lookback,
                                                WsHeader *hdr, bool withhold) {
   for (int e = threadIdx.x; e < E; e += kIdxThreads) {
@@ -243,21 +245,38 @@ __device__ __forceinline__ void block_lookback(int b, int E, const int *run, int
     int p = b - 1;
     uint64_t t0 = 0;
     while (p >= 0) {
-      uint64_t v = *(volatile uint64_t *)(lookback + (size_t)p * E + e);
-      uint64_t flag = v & 0xffffffff00000000ull;
-      if (flag == 0) {
-        uint64_t now = global_ns();
+      // the next kLookWindow predecessors' words at once, nearest first (before block 0: a zero
+      // prefix), then consumed in order up to the first prefix or the first word not yet published
+      uint64_t w[kLookWindow];
+#pragma unroll
+      for (int j = 0; j < kLookWindow; ++j)
+        w[j] = p - j >= 0 ? (uint64_t)*(volatile uint64_t *)(lookback + (size_t)(p - j) * E + e)
+                          : (uint64_t)kFlagPrefix;
+      int used = 0;
+      bool stop = false, stalled = false;
+#pragma unroll
+      for (int j = 0; j < kLookWindow; ++j) {
+        const uint64_t flag = w[j] & 0xffffffff00000000ull;
+        if (stop || stalled) continue;
+        if (flag == 0) {
+          stalled = true;
+          continue;
+        }
+        sum += (uint32_t)w[j];
+        ++used;
+        stop = flag == kFlagPrefix;
+      }
+      if (stop) break;
+      p -= used;
+      if (stalled) {
+        const uint64_t now = global_ns();
         if (t0 == 0) t0 = now;
         if (now - t0 > kWaitLimitNs) {
           report(hdr, MOE_ERR_DEVICE_TIMEOUT, b);
           break;
         }
         __nanosleep(64);
-        continue;
       }
-      sum += (uint32_t)v;
-      if (flag == kFlagPrefix) break;
-      --p;
     }
     excl[e] = (int)sum;
     if (!withhold) *mine = kFlagPrefix | (sum + agg);
