@@ -6,7 +6,8 @@
 // Here that is a stable counting sort of the T*k routing slots by expert id:
 //   count kernel : warp-aggregated (match.any) shared-memory histograms, one global atomic per
 //                  (block, expert); the last block to finish scans counts into offsets and tile offsets.
-//   index kernel : every block ranks its chunk of slots stably (match.any + per-warp counts), then
+//   index kernel : every block ranks its chunk of slots stably (each warp counts its own 128
+//                  consecutive slots per expert with match.any, then adds the earlier warps'), then
 //                  finds, per expert, how many earlier slots went to that expert with a decoupled
 //                  look-back over the preceding blocks (one 64-bit flag|value word per block and
 //                  expert), and scatters row_of_slot / token_of_row.
@@ -192,37 +193,43 @@ __global__ void __launch_bounds__(kIdxThreads) count_kernel(const int32_t *__res
 }
 
 // ---------------------------------------------------------------------------------------------
-// Stable ranks of a block's slots within their expert and the block's per-expert totals. key[i]
-// is the expert of the block's slot i * kIdxThreads + tid (-1: none). On return rank[i] counts the
-// block's earlier slots (in slot order) with the same expert and run[e] holds the block's count of
-// expert e. warp_cnt must be all zero on entry and is all zero again on return.
-__device__ __forceinline__ void block_ranks(const int (&key)[kIdxItems], int (&rank)[kIdxItems],
-                                            int (*warp_cnt)[MOE_MAX_EXPERTS], int *run, int E) {
+// Stable ranks of a block's slots within their expert and the block's per-expert totals. Warp w
+// owns the block's slots [32 ITEMS w, 32 ITEMS (w + 1)): key[i] is the expert of its slot
+// 32 ITEMS w + 32 i + lane (-1: none). A warp counts its slots per expert as it goes (match.any per
+// round of 32, no block barrier between rounds); the counts of the block's earlier warps are added
+// at the end. On return rank[i] counts the block's earlier slots (in slot order) with the same
+// expert and run[e] holds the block's count of expert e. warp_cnt must be all zero on entry; it is
+// left holding each warp's exclusive offsets.
+template <int ITEMS>
+__device__ __forceinline__ void warp_ranks(const int (&key)[ITEMS], int (&rank)[ITEMS],
+                                           int (*warp_cnt)[MOE_MAX_EXPERTS], int *run, int E) {
+  constexpr int kWarps = kIdxThreads / 32;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const unsigned lt_mask = (1u << lane) - 1u;
 #pragma unroll
-  for (int i = 0; i < kIdxItems; ++i) {
-    unsigned peers = __match_any_sync(0xffffffffu, key[i]);
-    int r_in_warp = __popc(peers & lt_mask);
-    bool leader = key[i] >= 0 && lane == __ffs(peers) - 1;
-    if (leader) warp_cnt[warp][key[i]] = __popc(peers);
-    __syncthreads();
-    for (int e = tid; e < E; e += kIdxThreads) {   // exclusive scan over warps, on top of earlier rounds
-      int r = run[e];
-#pragma unroll
-      for (int w = 0; w < kIdxThreads / 32; ++w) {
-        int c = warp_cnt[w][e];
-        warp_cnt[w][e] = r;
-        r += c;
-      }
-      run[e] = r;
-    }
-    __syncthreads();
-    rank[i] = key[i] >= 0 ? warp_cnt[warp][key[i]] + r_in_warp : 0;
-    __syncthreads();
-    for (int j = tid; j < (kIdxThreads / 32) * MOE_MAX_EXPERTS; j += kIdxThreads) (&warp_cnt[0][0])[j] = 0;
-    __syncthreads();
+  for (int i = 0; i < ITEMS; ++i) {
+    const unsigned peers = __match_any_sync(0xffffffffu, key[i]);
+    const int before = key[i] >= 0 ? warp_cnt[warp][key[i]] : 0;
+    rank[i] = before + __popc(peers & lt_mask);
+    __syncwarp();
+    if (key[i] >= 0 && lane == __ffs(peers) - 1) warp_cnt[warp][key[i]] = before + __popc(peers);
+    __syncwarp();
   }
+  __syncthreads();
+  for (int e = tid; e < E; e += kIdxThreads) {   // exclusive scan over the warps
+    int r = 0;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) {
+      const int c = warp_cnt[w][e];
+      warp_cnt[w][e] = r;
+      r += c;
+    }
+    run[e] = r;
+  }
+  __syncthreads();
+#pragma unroll
+  for (int i = 0; i < ITEMS; ++i)
+    if (key[i] >= 0) rank[i] += warp_cnt[warp][key[i]];
 }
 
 // Decoupled look-back: publish block b's per-expert aggregate run[e], walk back over the preceding
@@ -305,24 +312,24 @@ __global__ void __launch_bounds__(kIdxThreads) index_kernel(const int32_t *__res
   }
   __syncthreads();
   const int b = bid_s;
-  const int64_t base = (int64_t)b * kIdxChunk;
+  const int64_t base = (int64_t)b * kIdxChunk + (tid >> 5) * (32 * kIdxItems) + (tid & 31);   // slot of item 0
   int key[kIdxItems], rank[kIdxItems];
 #pragma unroll
-  for (int i = 0; i < kIdxItems; ++i) key[i] = slot_key(idx, base + i * kIdxThreads + tid, n, E, nullptr);
-  block_ranks(key, rank, warp_cnt, run, E);
+  for (int i = 0; i < kIdxItems; ++i) key[i] = slot_key(idx, base + 32 * i, n, E, nullptr);
+  warp_ranks<kIdxItems>(key, rank, warp_cnt, run, E);
   block_lookback(b, E, run, excl, lookback, hdr, b == hdr->armed - 1);
   __syncthreads();
 #pragma unroll
   for (int i = 0; i < kIdxItems; ++i) {
-    int64_t s = base + i * kIdxThreads + tid;
+    const int64_t s = base + 32 * i;
     if (s >= n) continue;
     if (key[i] < 0) {
       row_of_slot[s] = -1;
       continue;
     }
-    int row = row_base[key[i]] + excl[key[i]] + rank[i];
+    const int row = row_base[key[i]] + excl[key[i]] + rank[i];
     row_of_slot[s] = row;
-    token_of_row[row] = (int)(s / k);
+    token_of_row[row] = (int)s / k;   // s < T*k < 2^31
   }
   // padding rows of the grouped layout
   for (int e = blockIdx.x; e < E; e += gridDim.x) {
@@ -414,6 +421,7 @@ __global__ void __launch_bounds__(kIdxThreads) route_count_index_kernel(
   constexpr int kWarps = kIdxThreads / 32, kWarpSlots = 32 * ITEMS, kRciChunk = kIdxThreads * ITEMS;
   __shared__ int sk[kRciChunk];                            // experts of this block's slots, slot order
   __shared__ int warp_cnt[kWarps][MOE_MAX_EXPERTS];
+  __shared__ int run[MOE_MAX_EXPERTS];                     // this block's slots per expert
   __shared__ int excl[MOE_MAX_EXPERTS];                    // slots of each expert in blocks 0..b-1
   __shared__ int cnt[MOE_MAX_EXPERTS];                     // totals
   __shared__ int tile_first[MOE_MAX_EXPERTS + 1];          // exclusive scan of the tiles per expert
@@ -451,36 +459,20 @@ __global__ void __launch_bounds__(kIdxThreads) route_count_index_kernel(
   __syncthreads();
   // 2. stable ranks: a warp's running count per expert, then the earlier warps' counts
   int key[ITEMS], rank[ITEMS];
-  const unsigned lt_mask = (1u << lane) - 1u;
 #pragma unroll
   for (int i = 0; i < ITEMS; ++i) {
     const int64_t s = base + warp * kWarpSlots + i * 32 + lane;
     key[i] = s < send ? sk[s - base] : -1;
-    const unsigned peers = __match_any_sync(0xffffffffu, key[i]);
-    const int before = key[i] >= 0 ? warp_cnt[warp][key[i]] : 0;
-    rank[i] = before + __popc(peers & lt_mask);
-    __syncwarp();
-    if (key[i] >= 0 && lane == __ffs(peers) - 1) warp_cnt[warp][key[i]] = before + __popc(peers);
-    __syncwarp();
   }
-  __syncthreads();
-  // 3. publish: per-expert exclusive scan over the warps, the block's row of agg, the totals
+  warp_ranks<ITEMS>(key, rank, warp_cnt, run, E);
+  // 3. publish: the block's row of agg, the totals
   for (int e = tid; e < E; e += kIdxThreads) {
-    int r = 0;
-#pragma unroll
-    for (int w = 0; w < kWarps; ++w) {
-      const int c = warp_cnt[w][e];
-      warp_cnt[w][e] = r;
-      r += c;
-    }
+    const int r = run[e];
     agg[(size_t)b * E + e] = r;
     if (r) atomicAdd(acc + e, r);
   }
   __threadfence();
   __syncthreads();
-#pragma unroll
-  for (int i = 0; i < ITEMS; ++i)
-    if (key[i] >= 0) rank[i] += warp_cnt[warp][key[i]];
   if (tid == 0) {   // count in, then wait (bounded) for every block to have done the same
     atomicAdd(&hdr->tickets[0], 1u);
     bool ok = true;
