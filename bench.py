@@ -409,7 +409,7 @@ def run_ours(args):
         "kernels": kern,
         "e2e": {"value": round(job_tokens_per_s(world, w.T, args.steps, e2e_ms), 1), "unit": "tokens/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms / args.steps, 4),
-                "api": "HostPipeline.submit (pinned host inputs and results; copies overlap compute)"},
+                "api": "HostPipeline.submit (pinned host inputs and results; copies overlap compute; each slot's pass replayed from a CUDA graph)"},
         "gpu_launches": layer.launches(bwd) * args.steps,
         "clocks": clk.summary(),
         "cpu_baseline": cpu_base,

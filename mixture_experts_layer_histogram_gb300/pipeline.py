@@ -6,7 +6,9 @@ for a training pass) back to host memory. The copies run on two streams of their
 the neighbouring steps' compute: step i+1's inputs are uploaded while step i computes, and step
 i's results are downloaded while step i+1 computes. Device inputs and the layer's result tensors
 rotate over `depth` slots, so a copy never touches memory that a running kernel reads or writes;
-events order every reuse of a slot.
+events order every reuse of a slot. Each slot's pass is recorded once into a CUDA graph (on its
+first step, and again whenever the weight tensors change) and replayed, so a step costs the host
+one launch instead of one per kernel.
 
     pipe = HostPipeline(layer)
     for i, batch in enumerate(batches):      # dicts of pinned host tensors: x, logits (and g)
@@ -32,8 +34,11 @@ class StepResult:
 
 
 class HostPipeline:
-    def __init__(self, layer, depth=2):
+    def __init__(self, layer, depth=2, graphs=True):
+        """graphs: replay each slot's pass from a CUDA graph (False: launch the kernels one by one)."""
         self.layer = layer
+        self.graphs = graphs
+        self._graph = [None] * depth     # per slot: (weight pointers, graph)
         self.backward = layer.backward_enabled
         self.depth = depth
         dev = layer.device
@@ -95,10 +100,21 @@ class HostPipeline:
         self.compute.wait_event(self.in_ready[s])
         self.compute.wait_event(self.res_free[s])
         lay.out = res["out"]
-        lay.forward(inp["x"], inp.get("logits"), w_gate_up, w_down, self.compute, w_router=w_router)
         if self.backward:
             lay.dx, lay.d_logits = res["dx"], res["d_logits"]
-            lay.backward(inp["g"], w_gate_up, w_down, self.compute)
+        if self.graphs:
+            key = (w_gate_up.data_ptr(), w_down.data_ptr(), None if w_router is None else w_router.data_ptr())
+            if self._graph[s] is None or self._graph[s][0] != key:
+                with torch.cuda.stream(self.compute):   # the capture's warm-up passes follow the waits above
+                    graph = lay.capture(inp["x"], inp.get("logits"), w_gate_up, w_down,
+                                        grad_out=inp["g"] if self.backward else None, w_router=w_router)
+                self._graph[s] = (key, graph)
+            with torch.cuda.stream(self.compute):
+                self._graph[s][1].replay()
+        else:
+            lay.forward(inp["x"], inp.get("logits"), w_gate_up, w_down, self.compute, w_router=w_router)
+            if self.backward:
+                lay.backward(inp["g"], w_gate_up, w_down, self.compute)
         self.in_free[s].record(self.compute)
         self.res_ready[s].record(self.compute)
         self.d2h.wait_event(self.res_ready[s])
