@@ -44,8 +44,8 @@ METRIC_FWD = "MoE layer fwd tokens/s (E=64,k=8,d=2048); grouped-GEMM % BF16 peak
 # kernel changes, its traffic is unmeasured (null) until it is captured again.
 GEMM_SOURCES = ("gemm_rows.cu", "gemm_tc.cu", "tc_ptx.cuh", "tma_host.cuh", "common.cuh")
 GEMM_TRAFFIC = {    # workload -> (bytes per step, source digest)
-    "fwdbwd_t8192": (5756363008, "1a2a8dd03b616ac3"),
-    "fwd_t4096": (1219672320, "1a2a8dd03b616ac3"),
+    "fwdbwd_t8192": (5759519488, "1d603581913ada8f"),
+    "fwd_t4096": (1220222464, "1d603581913ada8f"),
 }
 DEFAULT_WORKLOAD = "fwdbwd_t8192"
 

@@ -55,6 +55,7 @@ constexpr int PRE = 16;
 
 struct Params {
   const int32_t *tile_offsets;
+  const int32_t *offsets;   // WGRAD: [E+1] exclusive scan of the routed row counts
   WsHeader *hdr;
   int E, d, f;
   int n_tiles;        // output tiles along N
@@ -499,13 +500,13 @@ __device__ __forceinline__ int div_small(int a, int b, float rb) {
 struct WgradWalker {
   int r, cluster, clusters, num_tiles, per, rank, bkp;
   float rper, rnt;
-  int s, e, k0, k1;   // the next tile and its expert's toff[e], toff[e + 1]
-  const int *toff, *order;
+  int s, e, k0, k1, c;   // the next tile, its expert's toff[e], toff[e + 1] and routed row count
+  const int *toff, *order, *offs;
 
   __device__ __forceinline__ WgradWalker(int cluster_, int clusters_, int num_tiles_, const Params &p,
                                          const int *toff_, const int *order_, int rank_, int bkp_)
       : r(0), cluster(cluster_), clusters(clusters_), num_tiles(num_tiles_), rank(rank_), bkp(bkp_), toff(toff_),
-        order(order_) {
+        order(order_), offs(p.offsets) {
     per = (p.m_tiles / 2) * p.n_tiles;
     rper = 1.0f / (float)per;
     rnt = 1.0f / (float)p.n_tiles;
@@ -517,6 +518,7 @@ struct WgradWalker {
     e = order[div_small(s, per, rper)];
     k0 = toff[e];
     k1 = toff[e + 1];
+    c = offs[e + 1] - offs[e];
   }
   __device__ __forceinline__ bool next(Tile &t, const Params &p) {
     if (s < 0) return false;
@@ -526,10 +528,11 @@ struct WgradWalker {
     t.m0 = m * (2 * BM) + rank * BM;
     t.n0 = (q - m * p.n_tiles) * BN;
     t.krow0 = k0 * BM;
-    t.kb = (k1 - k0) * (BM / bkp);
+    t.kb = (c + bkp - 1) / bkp;   // up to the last k-block that holds a routed row; the rest is zero padding
 #if MOE_CHECKS
-    // the expert's group is non-empty-or-empty in order, and the rows it reduces over lie inside the buffers
-    t.ok = k0 <= k1 && (int64_t)k1 * BM <= p.rows_max;
+    // the expert's group is non-empty-or-empty in order, its routed rows fit it, and the rows it
+    // reduces over lie inside the buffers
+    t.ok = k0 <= k1 && c >= 0 && c <= (k1 - k0) * BM && (int64_t)k1 * BM <= p.rows_max;
     if (!t.ok) t.kb = 0;
 #else
     t.ok = true;
@@ -853,6 +856,7 @@ int tc_grouped_ffn_bwd(const void *dy, const void *x, const int32_t *token_of_ro
   CUtensorMap mA, mB, mC;
   Params p{};
   p.tile_offsets = tile_offsets;
+  p.offsets = offsets;
   p.hdr = hdr;
   p.E = E;
   p.d = d;
